@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched Muon step on GB300.
+
+A step is one full ``muon_step_batched`` call (momentum + look-ahead + norm,
+10-iteration hybrid Newton–Schulz, scale + decoupled weight decay) over one
+batch of synthetic input.  The default workload is the stacked set:
+64 bf16 1024x1024 matrices with fp32 momentum, fresh Gaussian grads each
+step (sigma 1e-3, per-row scales log-uniform in [0.1, 10]), cycling through
+the 5 steps of grads; spectral scale, mu 0.95, lr 2.7e-4, wd 0.1.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload stack|single|heads]
+
+N > 1 runs one process per GPU (torchrun); each rank updates its own copy of
+the workload (matrices are independent units: weak scaling, no collective).
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "Muon-step params/s; Newton–Schulz TFLOP/s vs GB300 bf16 dense peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["stack", "single", "heads"], default="stack")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workloads (host-generated, seeded)
+# ---------------------------------------------------------------------------
+def build_workload(name: str, rank: int):
+    import workloads
+    if name == "stack":
+        st = workloads.stacked(seed=1 + 1000 * rank)
+        grads = [st.grad(t) for t in range(st.steps)]
+        return dict(kind="stack", W=st.W, M=st.M, grads=grads,
+                    desc=dict(workload="stack: 64 x bf16 1024x1024, fp32 momentum, 5-step grad cycle",
+                              matrices=64, rows=1024, cols=1024, w_dtype="bf16", g_dtype="bf16",
+                              m_dtype="fp32", schedule="8x(3.4445,-4.775,2.0315)+2x(2,-1.5,0.5)",
+                              scale="spectral", seed=1))
+    if name == "single":
+        s = workloads.single_matrix(seed=rank)
+        return dict(kind="single", W=s.W[None], M=s.M[None], grads=[s.G[None]],
+                    desc=dict(workload="single: fp32 256x512 with rank-4 spike", matrices=1,
+                              rows=256, cols=512, w_dtype="fp32", g_dtype="fp32", m_dtype="fp32",
+                              scale="spectral", seed=0))
+    h = workloads.split_heads(seed=2 + 1000 * rank)
+    return dict(kind="heads", W=h.W, M=h.M, grads=[h.G], n_heads=h.n_heads, head_dim=h.head_dim,
+                desc=dict(workload="heads: QKV 4096 x (32 x 128) bf16 split per head",
+                          matrices=32, rows=4096, cols=128, w_dtype="bf16", g_dtype="bf16",
+                          m_dtype="fp32", scale="spectral", seed=2))
+
+
+def make_groups(m, wl, Wd, Md, Gd):
+    if wl["kind"] == "heads":
+        return [[m.Group.split_head(Wd, g, Md, wl["n_heads"], wl["head_dim"])] for g in Gd]
+    return [[m.Group.stacked(Wd, g, Md)] for g in Gd]
+
+
+def n_params(wl):
+    return int(wl["W"].numel())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"muon_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = sorted(float(r[1]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = [n for k, n in enumerate(names) if any(r[5 + k].lower() == "active" for r in rows)]
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(rows[0][2]),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample
+# ---------------------------------------------------------------------------
+def oracle_sample(wl, seconds: float, min_units: int = 1):
+    import numpy as np
+    import oracle
+    W = wl["W"]
+    G = wl["grads"][0]
+    M = wl["M"]
+    hp = oracle.MuonHyper()
+    if wl["kind"] == "heads":
+        hd = wl["head_dim"]
+        mats = [(W[:, h * hd:(h + 1) * hd], G[:, h * hd:(h + 1) * hd], M[:, h * hd:(h + 1) * hd])
+                for h in range(wl["n_heads"])]
+        hp.fan_out_axis = 1
+    else:
+        mats = [(W[b], G[b], M[b]) for b in range(W.shape[0])]
+    done, params, t0 = 0, 0, time.perf_counter()
+    while done < min_units or (time.perf_counter() - t0 < seconds and done < len(mats)):
+        w, g, mm = mats[done % len(mats)]
+        oracle.muon_step(w.float().numpy().astype(np.float64), g.float().numpy().astype(np.float64),
+                         mm.numpy().astype(np.float64), hp)
+        done += 1
+        params += w.numel()
+    dt = time.perf_counter() - t0
+    return params / dt, done, dt
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    wl = build_workload(args.workload, 0)
+    per_step = 120.0 / max(1, args.steps + args.warmup)   # whole run ~2 min (>= 1 matrix/step)
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    t0 = time.perf_counter()
+    params = units = 0
+    for _ in range(args.steps):
+        v, n, dt = oracle_sample(wl, min(per_step, 10.0))
+        params += v * dt
+        units += n
+    dt = time.perf_counter() - t0
+    value = params / dt
+    rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
+    sample = f"{units} matrices of {rows}x{cols} over {args.steps} steps (float64 NumPy oracle)"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl["desc"],
+           "cpu_baseline": {"value": value, "unit": "params/s", "cores": cpu_cores(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("ns_gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "newton_schulz_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    if not e:
+        return None
+    return e.get("dram_bytes_per_launch_full_workload")
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import newton_schulz_02_gb300 as m
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m.load_library()
+    peaks, peak_src = load_peaks()
+
+    wl = build_workload(args.workload, rank)
+    Wd = wl["W"].to(dev)
+    Md = wl["M"].to(dev)
+    Gd = [g.to(dev) for g in wl["grads"]]
+    groups = make_groups(m, wl, Wd, Md, Gd)
+    hp = m.hparams()
+    ws = m.workspace(m.muon_step_workspace_size(groups[0]), device=dev)
+    P = n_params(wl)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        m.muon_step_batched(groups[i % len(groups)], hp, ws)
+    code, flags = m.muon_get_status(ws)
+    if code != m.MUON_OK or flags:
+        raise RuntimeError(f"device status {code} flags {flags:#x} after warm-up")
+
+    m.muon_profile_reset()
+    m.muon_profile_enable(True)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            m.muon_step_batched(groups[i % len(groups)], hp, ws)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    m.muon_profile_enable(False)
+    ms = start.elapsed_time(stop)
+    prof = m.muon_profile_query()
+    code, flags = m.muon_get_status(ws)
+    if code != m.MUON_OK or flags:
+        raise RuntimeError(f"device status {code} flags {flags:#x} after timed steps")
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * args.steps * P / (ms / 1e3)
+
+    # ---- per-kernel roofline (event-timed on the launching stream) --------
+    gemm = {k: prof[k] for k in ("ns_gram", "ns_poly", "ns_update") if prof[k]["launches"]}
+    ns_ms = sum(v["total_ms"] for v in gemm.values())
+    ns_flops = sum(v["alg_flops"] for v in gemm.values())
+    ns_tflops = ns_flops / (ns_ms / 1e3) / 1e12 if ns_ms > 0 else None
+    timed = {k: v for k, v in prof.items() if v["launches"] and v["total_ms"] > 0}
+    dom = max(timed, key=lambda k: timed[k]["total_ms"])
+    d = timed[dom]
+    avg_s = d["total_ms"] / d["launches"] / 1e3
+    if dom.startswith("ns_"):
+        per_launch = d["alg_flops"] / d["launches"]
+        achieved = per_launch / avg_s / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
+                "alg_flops_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
+                "traffic": read_traffic(dom), "peak_source": f"{peak_src} bf16 burst"}
+    else:
+        per_launch = d["alg_bytes"] / d["launches"]
+        achieved = per_launch / avg_s / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "alg_bytes_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
+                "peak_source": f"{peak_src} copy"}
+    kernels = {}
+    for k, v in timed.items():
+        e = {"launches": v["launches"], "total_ms": round(v["total_ms"], 4),
+             "share": round(v["total_ms"] / sum(x["total_ms"] for x in timed.values()), 4)}
+        if v["alg_flops"]:
+            e["tflops"] = round(v["alg_flops"] / (v["total_ms"] / 1e3) / 1e12, 2)
+        if v["alg_bytes"]:
+            e["gbs"] = round(v["alg_bytes"] / (v["total_ms"] / 1e3) / 1e9, 1)
+            e["hbm_frac_of_measured"] = round(e["gbs"] / peaks["hbm_gbs"], 3)
+        kernels[k] = e
+    launches = int(sum(v["launches"] for v in prof.values()))
+
+    # ---- end to end: host buffers, copies inside the timed region ------------
+    e2e = None
+    if args.e2e_steps > 0:
+        Gh = [g.pin_memory() for g in wl["grads"]]
+        Gslot = torch.empty_like(Gd[0])
+        Wh = torch.empty(Wd.shape, dtype=Wd.dtype).pin_memory()
+        eg = make_groups(m, wl, Wd, Md, [Gslot])[0]
+        flags_h = []
+        for i in range(2):
+            Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
+            m.muon_step_batched(eg, hp, ws)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.e2e_steps):
+            Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
+            m.muon_step_batched(eg, hp, ws)
+            Wh.copy_(Wd, non_blocking=True)
+            flags_h.append(m.muon_get_status(ws))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        if any(c != m.MUON_OK or f for c, f in flags_h):
+            raise RuntimeError("device status set during the end-to-end steps")
+        e2e = {"value": world * args.e2e_steps * P / (e_ms / 1e3), "unit": "params/s",
+               "h2d_bytes_per_step": int(Gslot.numel() * Gslot.element_size()),
+               "d2h_bytes_per_step": int(Wh.numel() * Wh.element_size() + 4),
+               "steps": args.e2e_steps, "wall_s": round(wall, 4),
+               "path": "pinned host G -> device, muon_step_batched, device W -> pinned host, "
+                       "status word read (synchronising) every step"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    cpu_v, cpu_n, cpu_dt = oracle_sample(wl, args.cpu_seconds)
+    rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
+    clocks = clk.summary()
+    desc = dict(wl["desc"])
+    desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
+                l2="inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M + 512 MiB workspace"
+                if wl["kind"] == "stack" else "small workload (L2-resident)")
+    out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded Gaussian grads, per-row scales)", "config": desc,
+           "ns_tflops": ns_tflops,
+           "ns_frac_of_bf16_peak": ns_tflops / peaks["bf16_tflops"] if ns_tflops else None,
+           "roofline": roof, "kernels": kernels,
+           "cpu_baseline": {"value": cpu_v, "unit": "params/s", "cores": cpu_cores(),
+                            "kind": "oracle",
+                            "sample": f"{cpu_n} matrices of {rows}x{cols}, one Muon step each, "
+                                      f"float64 NumPy, {cpu_dt:.1f} s"},
+           "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+           "peaks": dict(peaks, source=peak_src)}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    sys.path.insert(0, ROOT)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

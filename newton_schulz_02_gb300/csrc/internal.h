@@ -1,0 +1,122 @@
+// Internal interface between the C-ABI layer (muon_api.cu) and the kernels.
+// Not installed; the public interface is include/muon.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/muon.h"
+
+namespace muon {
+
+constexpr uint32_t kFlagNonFinite = MUON_FLAG_NONFINITE;
+constexpr uint32_t kFlagTimeout = MUON_FLAG_TIMEOUT;
+constexpr uint32_t kFlagMisaligned = MUON_FLAG_MISALIGNED;
+
+// Newton–Schulz work is done on the "wide" orientation n x m (n = min(rows,
+// cols), m = max), zero-padded to multiples of kPad in both dimensions so the
+// tensor-core kernels only ever see whole tiles.  Zero padding is exact: the
+// padded rows/columns of X, X X^T and of every later iterate stay zero.
+constexpr int kPad = 128;
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+enum PrepMode : int { kPrepMomentumSgd = 0, kPrepMomentumEma = 1, kPrepLoad = 2 };
+
+// Pass 1: momentum (+ look-ahead) or a plain load, writing the bf16 iterate
+// X into the workspace (wide orientation, padded) and per-block partial sums
+// of X^2 (fp32, from the fp32 value before the bf16 cast).
+struct PrepareArgs {
+  int batch, rows, cols;
+  int64_t row_stride;    // elements, of G, M and W
+  int64_t batch_stride;  // elements, used when g_ptrs == nullptr
+  int g_dtype;           // muon_dtype_t of the input (G, or X for newton_schulz_batched)
+  const void* const* g_ptrs;  // device array, or nullptr
+  const void* g_base;         // used when g_ptrs == nullptr
+  float* const* m_ptrs;       // momentum buffers (modes 0 and 1)
+  void* const* w_ptrs;        // only checked for alignment (may be nullptr)
+  int mode;
+  int nesterov;
+  float mu;            // sgd: mu; ema: beta
+  double ema_omb;      // ema: 1 - beta (exact, from the fp32 beta)
+  float c_mom, c_grad;  // ema look-ahead: X = c_mom*buf + c_grad*g
+  __nv_bfloat16* X;     // [batch][n_pad][m_pad]
+  int n_pad, m_pad;
+  int tall;             // rows > cols: X holds the transpose
+  int parts;            // blocks per matrix (partials per matrix)
+  float* partials;      // [batch][parts]
+  uint8_t* skip;        // [batch], set to 1 for a matrix with a misaligned pointer
+  uint32_t* status;
+};
+
+struct FinalizeArgs {
+  int batch, parts;
+  const float* partials;
+  const uint8_t* skip;
+  float* inv_s;  // [batch]: 1/||X||_F (0 for a zero or skipped matrix); 1 if !normalize
+  int normalize;
+  uint32_t* status;
+};
+
+// Last pass: W <- W*decay - lr_scale*O'  (mode 0), or out <- O' (mode 1).
+struct ApplyArgs {
+  int batch, rows, cols;
+  int64_t row_stride;        // W (mode 0)
+  int mode;
+  int w_dtype;               // W dtype (mode 0) / out dtype (mode 1)
+  void* const* w_ptrs;       // mode 0
+  void* out_base;            // mode 1: dense [batch][rows][cols]
+  const uint8_t* wd_mask;    // mode 0, may be nullptr
+  float decay_on;            // 1 - lr*wd
+  float lr_scale;            // lr * scale
+  const __nv_bfloat16* X;    // final iterate [batch][n_pad][m_pad]
+  int n_pad, m_pad, tall;
+  int parts;
+  const uint8_t* skip;
+  const float* oscale;       // per-matrix factor on O' (zero-iteration schedules), or nullptr
+};
+
+struct NsChainArgs {
+  int batch, n_pad, m_pad;
+  int n, m;             // unpadded sizes (algorithmic flop counts)
+  __nv_bfloat16* X0;
+  __nv_bfloat16* X1;
+  __nv_bfloat16* A;
+  __nv_bfloat16* B;
+  const float* inv_s;   // folded into the first iteration; nullptr = no normalisation
+  const float* coeffs;  // host [iters][3]
+  int iters;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// Kernel kinds for launch counting and event timing (prof.cu).
+enum KernelKind : int {
+  kKindPrepare = 0,
+  kKindFinalize,
+  kKindGram,
+  kKindPoly,
+  kKindUpdate,
+  kKindApply,
+  kKindTimeoutCheck,
+  kKindCount
+};
+void prof_begin(KernelKind k, cudaStream_t st);
+void prof_end(KernelKind k, cudaStream_t st, double alg_flops, double alg_bytes);
+
+int prepare_parts(int rows, int cols, int n_pad, int m_pad);
+int apply_parts(int rows, int cols);
+
+cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st);
+cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st);
+cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st);
+cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Runs the whole chain; the final iterate is left in X0 if the number of
+// iterations is even, else in X1.  Returns cudaErrorNotSupported when the
+// driver entry point for tensor maps is missing.
+cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st);
+
+}  // namespace muon

@@ -1,0 +1,455 @@
+// C ABI of the batched Muon step (declared in include/muon.h).
+//
+// Host side only: argument validation (everything the host can check is
+// checked before the first enqueue), shape grouping, workspace layout, and
+// the per-group launch sequence
+//   prepare (momentum / look-ahead / X -> workspace, partial sums of X^2)
+//   -> finalize (1/||X||_F per matrix)
+//   -> Newton–Schulz chain (tcgen05 GEMMs)
+//   -> apply (scale, decoupled weight decay, write W) or store O'.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+using namespace muon;
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+const muon_ns_stage_t kHybridStages[2] = {
+    {8, 3.4445f, -4.7750f, 2.0315f},  // "Muon 优化器" §2, fast stage
+    {2, 2.0f, -1.5f, 0.5f},           // stable stage
+};
+
+constexpr int kMaxDim = 1 << 20;
+constexpr size_t kHeaderBytes = 256;  // status word + reserved
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(int d) { return d == MUON_BF16 || d == MUON_F32; }
+
+int dsize(int d) { return d == MUON_BF16 ? 2 : 4; }
+
+struct Layout {
+  int n_pad = 0, m_pad = 0, parts = 0;
+  size_t x0 = 0, x1 = 0, a = 0, b = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
+};
+
+Layout layout_for(int batch, int rows, int cols) {
+  Layout L;
+  const int n = rows < cols ? rows : cols, m = rows < cols ? cols : rows;
+  L.n_pad = static_cast<int>(round_up(n, kPad));
+  L.m_pad = static_cast<int>(round_up(m, kPad));
+  L.parts = prepare_parts(rows, cols, L.n_pad, L.m_pad);
+  const size_t xb = static_cast<size_t>(batch) * L.n_pad * L.m_pad * 2;
+  const size_t sb = static_cast<size_t>(batch) * L.n_pad * L.n_pad * 2;
+  size_t off = kHeaderBytes;
+  L.x0 = off; off += align256(xb);
+  L.x1 = off; off += align256(xb);
+  L.a = off; off += align256(sb);
+  L.b = off; off += align256(sb);
+  L.partials = off; off += align256(static_cast<size_t>(batch) * L.parts * 4);
+  L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
+  L.skip = off; off += align256(static_cast<size_t>(batch));
+  L.total = off;
+  return L;
+}
+
+muon_status_t check_view(const muon_view_t& v) {
+  if (v.rows < 1 || v.cols < 1 || v.rows > kMaxDim || v.cols > kMaxDim) return MUON_ERR_INVALID_ARG;
+  if (v.row_stride < v.cols) return MUON_ERR_INVALID_ARG;
+  if (v.fan_out_axis != 0 && v.fan_out_axis != 1) return MUON_ERR_INVALID_ARG;
+  if (v.cols % 8 != 0) return MUON_ERR_UNSUPPORTED;
+  if (v.row_stride % 8 != 0) return MUON_ERR_MISALIGNED;
+  return MUON_OK;
+}
+
+muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* coeffs,
+                              int* normalize) {
+  muon_ns_schedule_t def;
+  if (s == nullptr) {
+    muon_ns_hybrid_schedule(&def);
+    s = &def;
+  }
+  if (s->prec == MUON_NS_TF32) return MUON_ERR_UNSUPPORTED;
+  if (s->prec != MUON_NS_BF16) return MUON_ERR_INVALID_ARG;
+  if (s->n_stages < 0 || (s->n_stages > 0 && s->stages == nullptr)) return MUON_ERR_INVALID_ARG;
+  if (s->normalize != 0 && s->normalize != 1) return MUON_ERR_INVALID_ARG;
+  coeffs->clear();
+  for (int i = 0; i < s->n_stages; ++i) {
+    const muon_ns_stage_t& st = s->stages[i];
+    if (st.steps < 0 || st.steps > 1000) return MUON_ERR_INVALID_ARG;
+    if (!std::isfinite(st.a) || !std::isfinite(st.b) || !std::isfinite(st.c))
+      return MUON_ERR_INVALID_ARG;
+    for (int k = 0; k < st.steps; ++k) {
+      coeffs->push_back(st.a);
+      coeffs->push_back(st.b);
+      coeffs->push_back(st.c);
+    }
+  }
+  *normalize = s->normalize;
+  return MUON_OK;
+}
+
+// Update scale (host, double): "Muon 优化器" Algorithm 1 (spectral) and
+// "Scaling for MuP over Muon optimizer" (unit_rms_norm).
+double update_scale(const muon_view_t& v, muon_scale_mode_t mode, float gamma) {
+  const double r = v.rows, c = v.cols;
+  switch (mode) {
+    case MUON_SCALE_SPECTRAL: return std::sqrt(r > c ? r : c) * static_cast<double>(gamma);
+    case MUON_SCALE_UNIT_RMS_NORM: {
+      const double fan_out = v.fan_out_axis == 0 ? r : c;
+      const double fan_in = v.fan_out_axis == 0 ? c : r;
+      return std::sqrt(fan_out / fan_in);
+    }
+    default: return 1.0;
+  }
+}
+
+muon_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA; }
+
+// Shared tail of both entry points: norm, NS chain, last pass.
+muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_view_t& v,
+                             const std::vector<float>& coeffs, int normalize, ApplyArgs ap,
+                             cudaStream_t st) {
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  FinalizeArgs fa{};
+  fa.batch = batch;
+  fa.parts = L.parts;
+  fa.partials = reinterpret_cast<const float*>(ws + L.partials);
+  fa.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
+  fa.inv_s = reinterpret_cast<float*>(ws + L.inv_s);
+  fa.normalize = normalize;
+  fa.status = status;
+  cudaError_t e = launch_finalize(fa, st);
+  if (e != cudaSuccess) return MUON_ERR_CUDA;
+
+  const int iters = static_cast<int>(coeffs.size() / 3);
+  NsChainArgs na{};
+  na.batch = batch;
+  na.n_pad = L.n_pad;
+  na.m_pad = L.m_pad;
+  na.n = v.rows < v.cols ? v.rows : v.cols;
+  na.m = v.rows < v.cols ? v.cols : v.rows;
+  na.X0 = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
+  na.X1 = reinterpret_cast<__nv_bfloat16*>(ws + L.x1);
+  na.A = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
+  na.B = reinterpret_cast<__nv_bfloat16*>(ws + L.b);
+  na.inv_s = normalize ? reinterpret_cast<const float*>(ws + L.inv_s) : nullptr;
+  na.coeffs = coeffs.data();
+  na.iters = iters;
+  na.status = status;
+  na.timeout_ns = g_timeout_ns.load();
+  e = run_ns_chain(na, st);
+  if (e == cudaErrorNotSupported) return MUON_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return MUON_ERR_CUDA;
+
+  ap.X = (iters % 2 == 0) ? na.X0 : na.X1;
+  ap.n_pad = L.n_pad;
+  ap.m_pad = L.m_pad;
+  ap.tall = v.rows > v.cols;
+  ap.parts = apply_parts(v.rows, v.cols);
+  ap.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
+  ap.oscale = (iters == 0 && normalize) ? reinterpret_cast<const float*>(ws + L.inv_s) : nullptr;
+  return cuda_status(launch_apply(ap, st));
+}
+
+muon_status_t check_workspace(const void* ws, size_t bytes, size_t need) {
+  if (ws == nullptr) return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MUON_ERR_MISALIGNED;
+  if (bytes < need) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  return MUON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+muon_status_t muon_ns_hybrid_schedule(muon_ns_schedule_t* out) {
+  if (out == nullptr) return MUON_ERR_INVALID_ARG;
+  out->stages = kHybridStages;
+  out->n_stages = 2;
+  out->normalize = 1;
+  out->prec = MUON_NS_BF16;
+  return MUON_OK;
+}
+
+muon_status_t muon_group_by_shape(const muon_tensor_desc_t* t, int n, int max_batch,
+                                  int* group_of_tensor, int* n_groups) {
+  if (n < 0 || max_batch < 0 || n_groups == nullptr) return MUON_ERR_INVALID_ARG;
+  if (n > 0 && (t == nullptr || group_of_tensor == nullptr)) return MUON_ERR_INVALID_ARG;
+  using Key = std::tuple<int, int, int64_t, int, int, int>;
+  std::vector<Key> order;
+  std::map<Key, std::vector<int>> members;
+  for (int i = 0; i < n; ++i) {
+    const Key k{t[i].rows, t[i].cols, t[i].row_stride, static_cast<int>(t[i].w_dtype),
+                static_cast<int>(t[i].g_dtype), t[i].fan_out_axis};
+    auto it = members.find(k);
+    if (it == members.end()) {
+      order.push_back(k);
+      members[k].push_back(i);
+    } else {
+      it->second.push_back(i);
+    }
+  }
+  int g = 0;
+  for (const Key& k : order) {
+    const std::vector<int>& idx = members[k];
+    const size_t step = max_batch == 0 ? idx.size() : static_cast<size_t>(max_batch);
+    for (size_t s = 0; s < idx.size(); s += step) {
+      for (size_t j = s; j < idx.size() && j < s + step; ++j) group_of_tensor[idx[j]] = g;
+      ++g;
+    }
+  }
+  *n_groups = g;
+  return MUON_OK;
+}
+
+muon_status_t muon_step_workspace_size(const muon_group_t* groups, int n_groups,
+                                       const muon_ns_schedule_t* schedule, size_t* bytes) {
+  if (bytes == nullptr || n_groups < 0 || (n_groups > 0 && groups == nullptr))
+    return MUON_ERR_INVALID_ARG;
+  std::vector<float> coeffs;
+  int normalize = 1;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize);
+  if (s != MUON_OK) return s;
+  size_t need = kHeaderBytes;
+  for (int i = 0; i < n_groups; ++i) {
+    if (groups[i].batch < 1) return MUON_ERR_INVALID_ARG;
+    s = check_view(groups[i].view);
+    if (s != MUON_OK) return s;
+    const Layout L = layout_for(groups[i].batch, groups[i].view.rows, groups[i].view.cols);
+    if (L.total > need) need = L.total;
+  }
+  *bytes = need;
+  return MUON_OK;
+}
+
+muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
+                                const muon_hparams_t* hp, const muon_ns_schedule_t* schedule,
+                                void* workspace, size_t workspace_bytes, muon_stream_t stream) {
+  if (hp == nullptr || n_groups < 0 || (n_groups > 0 && groups == nullptr))
+    return MUON_ERR_INVALID_ARG;
+  if (!std::isfinite(hp->mu) || !std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) ||
+      !std::isfinite(hp->gamma))
+    return MUON_ERR_INVALID_ARG;
+  if (hp->style != MUON_NESTEROV_SGD && hp->style != MUON_NESTEROV_EMA) return MUON_ERR_INVALID_ARG;
+  if (hp->nesterov != 0 && hp->nesterov != 1) return MUON_ERR_INVALID_ARG;
+  if (hp->scale_mode != MUON_SCALE_SPECTRAL && hp->scale_mode != MUON_SCALE_UNIT_RMS_NORM &&
+      hp->scale_mode != MUON_SCALE_NONE)
+    return MUON_ERR_INVALID_ARG;
+  if (hp->style == MUON_NESTEROV_EMA && (hp->t < 1 || hp->mu >= 1.f || hp->mu < 0.f))
+    return MUON_ERR_INVALID_ARG;
+  std::vector<float> coeffs;
+  int normalize = 1;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize);
+  if (s != MUON_OK) return s;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_group_t& g = groups[i];
+    if (g.batch < 1 || g.w_ptrs == nullptr || g.g_ptrs == nullptr || g.m_ptrs == nullptr)
+      return MUON_ERR_INVALID_ARG;
+    if (!valid_dtype(g.w_dtype) || !valid_dtype(g.g_dtype)) return MUON_ERR_INVALID_ARG;
+    s = check_view(g.view);
+    if (s != MUON_OK) return s;
+  }
+  size_t need = 0;
+  s = muon_step_workspace_size(groups, n_groups, schedule, &need);
+  if (s != MUON_OK) return s;
+  s = check_workspace(workspace, workspace_bytes, need);
+  if (s != MUON_OK) return s;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, kHeaderBytes, st) != cudaSuccess) return MUON_ERR_CUDA;
+
+  // 'ema' look-ahead coefficients, from the fp32 beta, in double.
+  const double beta = hp->mu;
+  double c_mom = 0.0, c_grad = 0.0;
+  if (hp->style == MUON_NESTEROV_EMA) {
+    const double t = static_cast<double>(hp->t);
+    if (hp->nesterov) {
+      c_mom = beta / (1.0 - std::pow(beta, t + 1.0));
+      c_grad = (1.0 - beta) / (1.0 - std::pow(beta, t));
+    } else {
+      c_mom = 1.0 / (1.0 - std::pow(beta, t));
+    }
+  }
+
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_group_t& g = groups[i];
+    const Layout L = layout_for(g.batch, g.view.rows, g.view.cols);
+    if (cudaMemsetAsync(ws + L.skip, 0, static_cast<size_t>(g.batch), st) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    PrepareArgs pa{};
+    pa.batch = g.batch;
+    pa.rows = g.view.rows;
+    pa.cols = g.view.cols;
+    pa.row_stride = g.view.row_stride;
+    pa.g_dtype = g.g_dtype;
+    pa.g_ptrs = g.g_ptrs;
+    pa.m_ptrs = g.m_ptrs;
+    pa.w_ptrs = g.w_ptrs;
+    pa.mode = hp->style == MUON_NESTEROV_SGD ? kPrepMomentumSgd : kPrepMomentumEma;
+    pa.nesterov = hp->nesterov;
+    pa.mu = hp->mu;
+    pa.ema_omb = 1.0 - beta;
+    pa.c_mom = static_cast<float>(c_mom);
+    pa.c_grad = static_cast<float>(c_grad);
+    pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
+    pa.n_pad = L.n_pad;
+    pa.m_pad = L.m_pad;
+    pa.tall = g.view.rows > g.view.cols;
+    pa.parts = L.parts;
+    pa.partials = reinterpret_cast<float*>(ws + L.partials);
+    pa.skip = reinterpret_cast<uint8_t*>(ws + L.skip);
+    pa.status = reinterpret_cast<uint32_t*>(ws);
+    if (launch_prepare(pa, st) != cudaSuccess) return MUON_ERR_CUDA;
+
+    const double scale = update_scale(g.view, hp->scale_mode, hp->gamma);
+    ApplyArgs ap{};
+    ap.batch = g.batch;
+    ap.rows = g.view.rows;
+    ap.cols = g.view.cols;
+    ap.row_stride = g.view.row_stride;
+    ap.mode = 0;
+    ap.w_dtype = g.w_dtype;
+    ap.w_ptrs = g.w_ptrs;
+    ap.wd_mask = g.wd_mask;
+    ap.decay_on = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+    ap.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
+    s = run_group_tail(L, ws, g.batch, g.view, coeffs, normalize, ap, st);
+    if (s != MUON_OK) return s;
+  }
+  return MUON_OK;
+}
+
+muon_status_t newton_schulz_workspace_size(const muon_view_t* view, int batch,
+                                           const muon_ns_schedule_t* schedule, size_t* bytes) {
+  if (view == nullptr || bytes == nullptr || batch < 1) return MUON_ERR_INVALID_ARG;
+  muon_status_t s = check_view(*view);
+  if (s != MUON_OK) return s;
+  std::vector<float> coeffs;
+  int normalize = 1;
+  s = expand_schedule(schedule, &coeffs, &normalize);
+  if (s != MUON_OK) return s;
+  *bytes = layout_for(batch, view->rows, view->cols).total;
+  return MUON_OK;
+}
+
+muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_view_t* view,
+                                    int batch, void* out, muon_dtype_t odt,
+                                    const muon_ns_schedule_t* schedule, void* workspace,
+                                    size_t workspace_bytes, muon_stream_t stream) {
+  if (x == nullptr || out == nullptr || view == nullptr || batch < 1) return MUON_ERR_INVALID_ARG;
+  if (!valid_dtype(xdt) || !valid_dtype(odt)) return MUON_ERR_INVALID_ARG;
+  muon_status_t s = check_view(*view);
+  if (s != MUON_OK) return s;
+  if (batch > 1 && view->batch_stride < 0) return MUON_ERR_INVALID_ARG;
+  if (view->batch_stride % 8 != 0) return MUON_ERR_MISALIGNED;
+  if (!aligned16(x) || !aligned16(out)) return MUON_ERR_MISALIGNED;
+  // x and out must not overlap
+  {
+    const char* xb = static_cast<const char*>(x);
+    const char* xe = xb + (static_cast<int64_t>(batch - 1) * view->batch_stride +
+                           static_cast<int64_t>(view->rows - 1) * view->row_stride + view->cols) *
+                              dsize(xdt);
+    const char* ob = static_cast<const char*>(out);
+    const char* oe = ob + static_cast<int64_t>(batch) * view->rows * view->cols * dsize(odt);
+    if (xb < oe && ob < xe) return MUON_ERR_INVALID_ARG;
+  }
+  std::vector<float> coeffs;
+  int normalize = 1;
+  s = expand_schedule(schedule, &coeffs, &normalize);
+  if (s != MUON_OK) return s;
+  const Layout L = layout_for(batch, view->rows, view->cols);
+  s = check_workspace(workspace, workspace_bytes, L.total);
+  if (s != MUON_OK) return s;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, kHeaderBytes, st) != cudaSuccess) return MUON_ERR_CUDA;
+  if (cudaMemsetAsync(ws + L.skip, 0, static_cast<size_t>(batch), st) != cudaSuccess)
+    return MUON_ERR_CUDA;
+
+  PrepareArgs pa{};
+  pa.batch = batch;
+  pa.rows = view->rows;
+  pa.cols = view->cols;
+  pa.row_stride = view->row_stride;
+  pa.batch_stride = view->batch_stride;
+  pa.g_dtype = xdt;
+  pa.g_base = x;
+  pa.mode = kPrepLoad;
+  pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
+  pa.n_pad = L.n_pad;
+  pa.m_pad = L.m_pad;
+  pa.tall = view->rows > view->cols;
+  pa.parts = L.parts;
+  pa.partials = reinterpret_cast<float*>(ws + L.partials);
+  pa.skip = reinterpret_cast<uint8_t*>(ws + L.skip);
+  pa.status = reinterpret_cast<uint32_t*>(ws);
+  if (launch_prepare(pa, st) != cudaSuccess) return MUON_ERR_CUDA;
+
+  ApplyArgs ap{};
+  ap.batch = batch;
+  ap.rows = view->rows;
+  ap.cols = view->cols;
+  ap.mode = 1;
+  ap.w_dtype = odt;
+  ap.out_base = out;
+  return run_group_tail(L, ws, batch, *view, coeffs, normalize, ap, st);
+}
+
+muon_status_t muon_get_status(const void* workspace, muon_stream_t stream, uint32_t* flags) {
+  if (workspace == nullptr || flags == nullptr) return MUON_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MUON_ERR_CUDA;
+  *flags = v;
+  return (v & MUON_FLAG_TIMEOUT) ? MUON_ERR_TIMEOUT : MUON_OK;
+}
+
+muon_status_t muon_set_wait_timeout_ns(uint64_t ns) {
+  if (ns == 0) return MUON_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns);
+  return MUON_OK;
+}
+
+muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
+                                      uint64_t timeout_ns, muon_stream_t stream) {
+  muon_status_t s = check_workspace(workspace, workspace_bytes, kHeaderBytes);
+  if (s != MUON_OK) return s;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return MUON_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kHeaderBytes, st) != cudaSuccess) return MUON_ERR_CUDA;
+  return cuda_status(
+      launch_wait_timeout_check(static_cast<uint32_t*>(workspace), timeout_ns, st));
+}
+
+const char* muon_status_string(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "MUON_OK";
+    case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG";
+    case MUON_ERR_MISALIGNED: return "MUON_ERR_MISALIGNED";
+    case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED";
+    case MUON_ERR_WORKSPACE_TOO_SMALL: return "MUON_ERR_WORKSPACE_TOO_SMALL";
+    case MUON_ERR_CUDA: return "MUON_ERR_CUDA";
+    case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT";
+  }
+  return "MUON_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,479 @@
+// Newton–Schulz chain on 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// One iteration of "Muon 优化器" (DeepSeek-V4 tech notes) §2,
+//     X <- a X + b (X X^T) X + c (X X^T)^2 X,
+// runs as three batched GEMMs on the wide, zero-padded bf16 iterate X (n x m):
+//
+//   Gram    S = X X^T            n x n, K = m  (symmetric: upper tiles + mirror)
+//   Poly    P = b S + c S S      n x n, K = n  (symmetric: upper tiles + mirror)
+//   Update  X' = a X + P X       n x m, K = n
+//
+// so that  a X + b S X + c S^2 X = a X + (b S + c S^2) X.  When c == 0 the
+// Poly GEMM is skipped and the Update uses S with weight b.  The Frobenius
+// normalisation is folded into the first iteration: with s = ||X||_F,
+// S_0 = (X X^T)/s^2 and X_1 = (a X + P_0 X)/s.
+//
+// Kernel shape (one persistent CTA per SM, 6 warps):
+//   warp 0      one thread issues TMA loads of A and B k-blocks into a
+//               multi-stage shared-memory ring (128-byte swizzle);
+//   warp 1      allocates TMEM and one thread issues tcgen05.mma
+//               (M=128, N=BN, K=16, bf16 -> fp32) into one of two TMEM
+//               accumulators, committing to mbarriers;
+//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes, fp32 epilogue
+//               math, bf16 stores (and the mirrored store of symmetric tiles).
+// The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// All operands are bf16 with fp32 accumulation; outputs are rounded to bf16.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace muon {
+namespace {
+
+constexpr int kBM = 128;  // tile rows (TMEM lanes)
+constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kGemmThreads = 192;
+
+enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2 };
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;
+  static constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct GemmParams {
+  int M, N, K;
+  int tiles_m, tiles_n, tiles_per_matrix, total_tiles;
+  __nv_bfloat16* out;
+  int64_t out_ld, out_bstride;
+  const __nv_bfloat16* aux;
+  int64_t aux_ld, aux_bstride;
+  float ca, cb, cc;
+  const float* mscale;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+// Tile t -> (matrix, tile row, tile column).  For symmetric outputs only the
+// tiles on or above the diagonal of BN x BN super-blocks are enumerated.
+template <int BN, bool SYM>
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& b, int& tm, int& tn) {
+  b = t / p.tiles_per_matrix;
+  int l = t - b * p.tiles_per_matrix;
+  if (!SYM) {
+    tm = l / p.tiles_n;
+    tn = l - tm * p.tiles_n;
+    return;
+  }
+  constexpr int R = BN / kBM;
+  const int S = p.tiles_n;
+  tn = 0;
+  for (tm = 0; tm < p.tiles_m; ++tm) {
+    const int cnt = S - tm / R;
+    if (l < cnt) {
+      tn = tm / R + l;
+      return;
+    }
+    l -= cnt;
+  }
+}
+
+// A drain wait: ignores the abort flag, still bounded.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) {
+      atomicOr(status, kFlagTimeout);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = s[q];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(h[k]);
+      v[q * 8 + 2 * k] = f.x;
+      v[q * 8 + 2 * k + 1] = f.y;
+    }
+  }
+}
+
+template <int BN, bool B_MN, int EPI, bool SYM>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const GemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, B_MN);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages * C::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4 * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nkb = p.K / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+        int b, tm, tn;
+        decode_tile<BN, SYM>(p, t, b, tm, tn);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          tma_load_3d(smA + stage * C::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM, b);
+          if (!B_MN) {
+            tma_load_3d(smB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN, b);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(smB + stage * C::kBBytes + j * (64 * kBK * 2), &tmB, &full[stage],
+                          tn * BN + j * 64, kb * kBK, b);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load this thread issued must land before the CTA exits.
+      for (int s = 0; s < kStages; ++s)
+        if ((issued >> s) & 1u) mbar_wait_drain(&full[s], (last_par >> s) & 1u, p.status, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smA + stage * C::kABytes);
+          const uint32_t b_addr = smem_u32(smB + stage * C::kBBytes);
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            // K-major A: 128 rows x 128 B, 8-row groups 1024 B apart; a 16-wide
+            // k step is 32 B along the swizzled row.
+            const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+            uint64_t bd;
+            if (B_MN) {
+              // MN-major B: 64-element (128 B) wide atoms of kBK k-rows,
+              // atoms kBK*128 B apart (LBO), 8 k-rows 1024 B apart (SBO);
+              // a 16-deep k step is 16 rows = 2048 B.
+              bd = smem_desc_sw128(b_addr + ks * 16 * 128, kBK * 128, 1024);
+            } else {
+              bd = smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+            }
+            tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs issued by this thread complete before teardown.
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0, p.status, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter accessible to this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      int b, tm, tn;
+      decode_tile<BN, SYM>(p, t, b, tm, tn);
+      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      const int row = tm * kBM + q * 32 + lane;
+      const bool mirror = SYM && (tn > tm / (BN / kBM));
+      float ms = 1.f;
+      if (p.mscale != nullptr) ms = p.mscale[b];
+      __nv_bfloat16* out = p.out + static_cast<int64_t>(b) * p.out_bstride;
+      const __nv_bfloat16* aux =
+          (EPI == kEpiGram) ? nullptr : p.aux + static_cast<int64_t>(b) * p.aux_bstride;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_ld_wait(r);
+        const int col0 = tn * BN + c * 32;
+        float v[32];
+        if (EPI == kEpiGram) {
+          const float s2 = ms * ms;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s2;
+        } else {
+          float x[32];
+          load_bf16x32(aux + static_cast<int64_t>(row) * p.aux_ld + col0, x);
+          if (EPI == kEpiPoly) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cc, __uint_as_float(r[e]), p.cb * x[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              v[e] = fmaf(p.cb, __uint_as_float(r[e]), p.ca * x[e]) * ms;
+          }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * p.out_ld + col0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 u;
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+          dst[k] = u;
+        }
+        if (mirror) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = __float2bfloat16_rn(v[e]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// K-major operand: [batch][rows][K] bf16, box = 64 (K) x box_rows.
+bool map_kmajor(CUtensorMap* m, const void* base, int batch, int rows, int K, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2,
+                                 static_cast<cuuint64_t>(rows) * K * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// MN-major operand: [batch][K rows][N cols] bf16, box = 64 (N) x 64 (K).
+bool map_mnmajor(CUtensorMap* m, const void* base, int batch, int K, int N) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2,
+                                 static_cast<cuuint64_t>(K) * N * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBK), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool B_MN, int EPI, bool SYM>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                        double alg_flops, cudaStream_t st) {
+  auto kern = k_ns_gemm<BN, B_MN, EPI, SYM>;
+  const size_t smem = Cfg<BN>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = std::max(1, std::min(p.total_tiles, sm_count()));
+  const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
+  prof_begin(kind, st);
+  kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+  prof_end(kind, st, alg_flops, 0.0);
+  return cudaGetLastError();
+}
+
+struct OperandMaps {
+  CUtensorMap k128, kbn, mn;
+};
+
+}  // namespace
+
+cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
+  if (a.iters == 0) return cudaSuccess;
+  if (encode_fn() == nullptr) return cudaErrorNotSupported;
+  const int n = a.n_pad, m = a.m_pad, batch = a.batch;
+  const int bn_sq = (n % 256 == 0) ? 256 : 128;
+  const int bn_up = (m % 256 == 0) ? 256 : 128;
+
+  OperandMaps X[2], S, P;
+  __nv_bfloat16* xb[2] = {a.X0, a.X1};
+  for (int i = 0; i < 2; ++i) {
+    if (!map_kmajor(&X[i].k128, xb[i], batch, n, m, kBM) ||
+        !map_kmajor(&X[i].kbn, xb[i], batch, n, m, bn_sq) ||
+        !map_mnmajor(&X[i].mn, xb[i], batch, n, m))
+      return cudaErrorInvalidValue;
+  }
+  if (!map_kmajor(&S.k128, a.A, batch, n, n, kBM) || !map_kmajor(&S.kbn, a.A, batch, n, n, bn_sq) ||
+      !map_kmajor(&P.k128, a.B, batch, n, n, kBM) || !map_kmajor(&P.kbn, a.B, batch, n, n, bn_sq))
+    return cudaErrorInvalidValue;
+
+  // Algorithmic flops per launch (unpadded n x m, symmetric products at half
+  // their dense count): Gram n^2 m, polynomial n^3, update 2 n^2 m per matrix.
+  const double nr = a.n, mr = a.m;
+  const double f_gram = batch * nr * nr * mr, f_poly = batch * nr * nr * nr,
+               f_update = 2.0 * batch * nr * nr * mr;
+  const int tm_sq = n / kBM;
+  const int S_sq = n / bn_sq;
+  const int sym_tiles = (bn_sq / kBM) * S_sq * (S_sq + 1) / 2;
+
+  for (int it = 0; it < a.iters; ++it) {
+    const float ca = a.coeffs[3 * it], cb = a.coeffs[3 * it + 1], cc = a.coeffs[3 * it + 2];
+    const int cur = it & 1;
+    const bool first = (it == 0);
+    cudaError_t e;
+
+    GemmParams g{};
+    g.M = n; g.N = n; g.K = m;
+    g.tiles_m = tm_sq; g.tiles_n = S_sq; g.tiles_per_matrix = sym_tiles;
+    g.total_tiles = sym_tiles * batch;
+    g.out = a.A; g.out_ld = n; g.out_bstride = static_cast<int64_t>(n) * n;
+    g.mscale = first ? a.inv_s : nullptr;
+    g.status = a.status; g.timeout_ns = a.timeout_ns;
+    e = (bn_sq == 256) ? launch_gemm<256, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, g, f_gram, st)
+                       : launch_gemm<128, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, g, f_gram, st);
+    if (e != cudaSuccess) return e;
+
+    if (cc != 0.f) {
+      GemmParams q = g;
+      q.K = n;
+      q.out = a.B;
+      q.aux = a.A; q.aux_ld = n; q.aux_bstride = static_cast<int64_t>(n) * n;
+      q.cb = cb; q.cc = cc;
+      q.mscale = nullptr;
+      e = (bn_sq == 256) ? launch_gemm<256, false, kEpiPoly, true>(S.k128, S.kbn, q, f_poly, st)
+                         : launch_gemm<128, false, kEpiPoly, true>(S.k128, S.kbn, q, f_poly, st);
+      if (e != cudaSuccess) return e;
+    }
+
+    GemmParams u{};
+    u.M = n; u.N = m; u.K = n;
+    u.tiles_m = n / kBM; u.tiles_n = m / bn_up; u.tiles_per_matrix = u.tiles_m * u.tiles_n;
+    u.total_tiles = u.tiles_per_matrix * batch;
+    u.out = xb[cur ^ 1]; u.out_ld = m; u.out_bstride = static_cast<int64_t>(n) * m;
+    u.aux = xb[cur]; u.aux_ld = m; u.aux_bstride = static_cast<int64_t>(n) * m;
+    u.ca = ca; u.cb = (cc != 0.f) ? 1.f : cb; u.cc = 0.f;
+    u.mscale = first ? a.inv_s : nullptr;
+    u.status = a.status; u.timeout_ns = a.timeout_ns;
+    const CUtensorMap& lhs = (cc != 0.f) ? P.k128 : S.k128;
+    e = (bn_up == 256) ? launch_gemm<256, true, kEpiUpdate, false>(lhs, X[cur].mn, u, f_update, st)
+                       : launch_gemm<128, true, kEpiUpdate, false>(lhs, X[cur].mn, u, f_update, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace muon

@@ -1,0 +1,294 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs.
+
+Tolerances (element by element, per matrix):
+  O'  (bf16 Newton–Schulz)  relative Frobenius error <= 3e-2
+  M   (fp32 momentum)       within 1 ulp of the correctly rounded oracle value
+  W                         max-abs <= 1e-2*lr*scale, plus half a bf16 ulp when
+                            W is stored in bf16 (the rounding of the store)
+"""
+import numpy as np
+import pytest
+import torch
+
+import newton_schulz_02_gb300 as m
+import oracle
+import workloads
+from tests.gpu_util import F32, check_w, f64, hyper, momentum_ref_f32, rel_fro, ulp_diff_f32
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+NS_TOL = 3e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.load_library()
+    torch.cuda.set_device(0)
+
+
+def run_ns(x: torch.Tensor, schedule=None, out_dtype=torch.float32):
+    """x: [batch, rows, cols] on the device."""
+    out = torch.empty(x.shape, dtype=out_dtype, device=DEV)
+    ws = m.workspace(m.newton_schulz_workspace_size(x.shape[1], x.shape[2], x.shape[0], schedule))
+    m.newton_schulz_batched(x, out, ws, schedule)
+    code, flags = m.muon_get_status(ws)
+    assert code == m.MUON_OK and flags == 0, (code, flags)
+    return out
+
+
+def oracle_ns_batch(x: torch.Tensor, stages=oracle.HYBRID_STAGES, normalize=True):
+    return [oracle.newton_schulz(f64(x[b]), stages, normalize) for b in range(x.shape[0])]
+
+
+# ---------------------------------------------------------------------------
+# Newton–Schulz alone
+# ---------------------------------------------------------------------------
+NS_SHAPES = [(256, 512), (512, 256), (200, 328), (328, 200), (128, 128), (384, 640),
+             (640, 384), (8, 8), (1, 64), (72, 8), (1024, 1024)]
+
+
+@pytest.mark.parametrize("rows,cols", NS_SHAPES)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ns_hybrid_matches_oracle(rows, cols, dtype):
+    rng = np.random.default_rng(rows * 1000 + cols)
+    batch = 3 if rows * cols <= 400_000 else 2
+    x = torch.tensor(rng.standard_normal((batch, rows, cols)) * 1e-3, dtype=dtype).to(DEV)
+    got = run_ns(x)
+    want = oracle_ns_batch(x)
+    for b in range(batch):
+        err = rel_fro(f64(got[b]), want[b])
+        assert err <= NS_TOL, (b, err)
+
+
+ISOLATING_SCHEDULES = {
+    "identity": [(1, (1.0, 0.0, 0.0))],        # X/||X||: load, norm, update epilogue
+    "gram": [(1, (0.0, 1.0, 0.0))],            # (X X^T) X: Gram + update (poly skipped)
+    "square": [(1, (0.0, 0.0, 1.0))],          # (X X^T)^2 X: Gram + poly + update
+    "mixed": [(1, (0.5, -0.25, 0.125))],
+    "two": [(2, (1.5, -0.5, 0.0))],
+}
+
+
+@pytest.mark.parametrize("name", sorted(ISOLATING_SCHEDULES))
+@pytest.mark.parametrize("rows,cols", [(256, 512), (384, 256), (512, 512)])
+def test_ns_single_stage_schedules(name, rows, cols):
+    stages = ISOLATING_SCHEDULES[name]
+    sched = m.Schedule(stages)
+    rng = np.random.default_rng(7)
+    x = torch.tensor(rng.standard_normal((2, rows, cols)), dtype=torch.bfloat16).to(DEV)
+    got = run_ns(x, sched)
+    want = oracle_ns_batch(x, stages)
+    for b in range(2):
+        assert rel_fro(f64(got[b]), want[b]) <= 1.5e-2
+
+
+def test_ns_without_normalisation_fixes_orthonormal_rows():
+    """Stable stage alone, no normalisation: rows of Q orthonormal stay put
+    (p(1) = 1, p'(1) = 0)."""
+    rng = np.random.default_rng(3)
+    Q, _ = np.linalg.qr(rng.standard_normal((512, 256)))
+    x = torch.tensor(Q.T[None], dtype=torch.float32).to(DEV)          # 256 x 512
+    sched = m.Schedule([(2, (2.0, -1.5, 0.5))], normalize=False)
+    got = f64(run_ns(x, sched)[0])
+    assert rel_fro(got, Q.T) <= 1e-2
+
+
+def test_ns_zero_input_gives_zero():
+    x = torch.zeros(2, 256, 384, dtype=torch.bfloat16, device=DEV)
+    got = run_ns(x)
+    assert torch.count_nonzero(got).item() == 0
+
+
+def test_ns_zero_iterations_is_normalisation():
+    rng = np.random.default_rng(11)
+    x = torch.tensor(rng.standard_normal((1, 128, 256)), dtype=torch.float32).to(DEV)
+    got = f64(run_ns(x, m.Schedule([]))[0])
+    want = f64(x[0]) / np.linalg.norm(f64(x[0]))
+    assert rel_fro(got, want) <= 5e-3
+
+
+def test_ns_strided_input_view():
+    """Matrices read through a view with row_stride > cols and a batch stride."""
+    rng = np.random.default_rng(12)
+    big = torch.tensor(rng.standard_normal((512, 1024)), dtype=torch.bfloat16).to(DEV)
+    view = m.muon_view_t(512, 256, 1024, 256, 0)          # 4 heads of 512 x 256
+    out = torch.empty(4, 512, 256, dtype=torch.float32, device=DEV)
+    ws = m.workspace(m.newton_schulz_workspace_size(512, 256, 4))
+    m.newton_schulz_batched(big, out, ws, view=view, batch=4)
+    torch.cuda.synchronize()
+    for h in range(4):
+        want = oracle.newton_schulz(f64(big[:, 256 * h:256 * (h + 1)]))
+        assert rel_fro(f64(out[h]), want) <= NS_TOL
+
+
+def test_ns_batched_equals_unbatched_bitwise():
+    rng = np.random.default_rng(13)
+    x = torch.tensor(rng.standard_normal((5, 256, 640)), dtype=torch.bfloat16).to(DEV)
+    whole = run_ns(x)
+    for b in range(5):
+        one = run_ns(x[b:b + 1].clone())
+        assert torch.equal(one[0], whole[b])
+
+
+# ---------------------------------------------------------------------------
+# the full step
+# ---------------------------------------------------------------------------
+def step_once(groups, hp_kw, schedule=None):
+    hp = m.hparams(**hp_kw)
+    ws = m.workspace(m.muon_step_workspace_size(groups, schedule))
+    m.muon_step_batched(groups, hp, ws, schedule)
+    code, flags = m.muon_get_status(ws)
+    return code, flags
+
+
+def test_single_fp32_matrix_step():
+    """One fp32 256x512 matrix with a rank-4 spike, zero momentum, spectral."""
+    case = workloads.single_matrix(seed=0)
+    W0, G0, M0 = f64(case.W), f64(case.G), f64(case.M)
+    W, G, M = case.W.to(DEV), case.G.to(DEV), case.M.to(DEV)
+    code, flags = step_once([m.Group([W], [G], [M])], case.hp)
+    assert code == m.MUON_OK and flags == 0
+    hp = hyper()
+    ref = oracle.muon_step(W0, G0, M0, hp)
+    assert np.max(ulp_diff_f32(M.cpu().numpy(), momentum_ref_f32(M0, G0, hp))) <= 1
+    check_w(f64(W), ref["W"], hp, ref["scale"], bf16=False)
+
+
+@pytest.mark.parametrize("style,nesterov,scale_mode", [
+    ("sgd", True, "spectral"), ("sgd", False, "unit_rms_norm"), ("ema", True, "spectral"),
+    ("ema", False, "none")])
+@pytest.mark.parametrize("rows,cols", [(256, 384), (384, 256)])
+def test_step_variants_fp32(style, nesterov, scale_mode, rows, cols):
+    W, G, M = workloads.random_case(21, rows, cols, batch=2, g_dtype=torch.float32,
+                                    w_dtype=torch.float32, m_scale=5.0)
+    W0, G0, M0 = f64(W), f64(G), f64(M)
+    Wd, Gd, Md = W.to(DEV), G.to(DEV), M.to(DEV)
+    for t in (1, 2):
+        kw = dict(style=style, nesterov=nesterov, scale_mode=scale_mode, t=t)
+        Mprev = f64(Md)
+        Wprev = f64(Wd)
+        code, flags = step_once([m.Group.stacked(Wd, Gd, Md)], kw)
+        assert code == m.MUON_OK and flags == 0
+        hp = hyper(style=style, nesterov=nesterov, scale_mode=scale_mode, t=t)
+        for b in range(2):
+            ref = oracle.muon_step(Wprev[b], G0[b], Mprev[b], hp)
+            assert np.max(ulp_diff_f32(Md[b].cpu().numpy(),
+                                       momentum_ref_f32(Mprev[b], G0[b], hp))) <= 1
+            check_w(f64(Wd[b]), ref["W"], hp, ref["scale"], bf16=False)
+
+
+def test_stacked_bf16_steps_and_ragged_shapes():
+    """Several groups in one call (square, wide ragged, tall ragged), bf16 W/G,
+    two steps with the state carried over."""
+    shapes = [(4, 512, 512), (3, 200, 328), (2, 328, 200)]
+    cases = [workloads.random_case(30 + i, r, c, batch=b) for i, (b, r, c) in enumerate(shapes)]
+    dev = [(W.to(DEV), G.to(DEV), M.to(DEV)) for W, G, M in cases]
+    groups = [m.Group.stacked(W, G, M) for W, G, M in dev]
+    hp = hyper()
+    for step in range(2):
+        prev = [(f64(W), f64(G), f64(M)) for W, G, M in dev]
+        code, flags = step_once(groups, {})
+        assert code == m.MUON_OK and flags == 0
+        for (W, G, M), (W0, G0, M0) in zip(dev, prev):
+            for b in range(W.shape[0]):
+                ref = oracle.muon_step(W0[b], G0[b], M0[b], hp)
+                assert np.max(ulp_diff_f32(M[b].cpu().numpy(), momentum_ref_f32(M0[b], G0[b], hp))) <= 1
+                check_w(f64(W[b]), ref["W"], hp, ref["scale"], bf16=True)
+
+
+def test_weight_decay_mask():
+    W, G, M = workloads.random_case(40, 256, 256, batch=2, w_dtype=torch.float32)
+    W0, G0, M0 = f64(W), f64(G), f64(M)
+    Wd, Gd, Md = W.to(DEV), G.to(DEV), M.to(DEV)
+    code, flags = step_once([m.Group.stacked(Wd, Gd, Md, wd_mask=[True, False])], {})
+    assert code == m.MUON_OK and flags == 0
+    hp = hyper()
+    for b, decay in enumerate([True, False]):
+        ref = oracle.muon_step(W0[b], G0[b], M0[b], hp, decay=decay)
+        check_w(f64(Wd[b]), ref["W"], hp, ref["scale"], bf16=False)
+
+
+def test_zero_gradient_is_pure_weight_decay():
+    W = torch.tensor(np.random.default_rng(41).normal(0, 0.02, (1, 256, 512)), dtype=torch.float32)
+    Wd = W.to(DEV)
+    Gd = torch.zeros_like(Wd)
+    Md = torch.zeros_like(Wd)
+    code, flags = step_once([m.Group.stacked(Wd, Gd, Md)], {})
+    assert code == m.MUON_OK and flags == 0
+    decay = np.float32(1.0 - float(np.float32(2.7e-4)) * float(np.float32(0.1)))
+    want = (W.numpy() * decay).astype(np.float32)
+    assert np.max(ulp_diff_f32(Wd.cpu().numpy(), want)) <= 1
+    assert torch.count_nonzero(Md).item() == 0
+
+
+def test_batched_equals_unbatched_and_chunking_bitwise():
+    W, G, M = workloads.random_case(42, 256, 384, batch=6)
+    runs = []
+    for chunks in ([6], [1] * 6, [2, 2, 2], [4, 2]):
+        Wd, Gd, Md = W.clone().to(DEV), G.to(DEV), M.clone().to(DEV)
+        groups, start = [], 0
+        for c in chunks:
+            groups.append(m.Group.stacked(Wd[start:start + c], Gd[start:start + c], Md[start:start + c]))
+            start += c
+        code, flags = step_once(groups, {})
+        assert code == m.MUON_OK and flags == 0
+        runs.append((Wd.cpu(), Md.cpu()))
+    for Wr, Mr in runs[1:]:
+        assert torch.equal(Wr, runs[0][0]) and torch.equal(Mr, runs[0][1])
+
+
+@pytest.mark.parametrize("scale_mode", ["spectral", "unit_rms_norm"])
+def test_split_head_attention_weight(scale_mode):
+    """QKV weight 4096 x (32 x 128), orthogonalised per head (heads = batch,
+    fan_out = head size 128)."""
+    h = workloads.split_heads(seed=2)
+    W0, G0, M0 = f64(h.W), f64(h.G), f64(h.M)
+    Wd, Gd, Md = h.W.to(DEV), h.G.to(DEV), h.M.to(DEV)
+    code, flags = step_once([m.Group.split_head(Wd, Gd, Md, h.n_heads, h.head_dim)],
+                            dict(scale_mode=scale_mode))
+    assert code == m.MUON_OK and flags == 0
+    hp = hyper(scale_mode=scale_mode, fan_out_axis=1)
+    Wg, Mg = f64(Wd), Md.cpu().numpy()
+    for k in range(h.n_heads):
+        s = slice(k * h.head_dim, (k + 1) * h.head_dim)
+        ref = oracle.muon_step(W0[:, s], G0[:, s], M0[:, s], hp)
+        assert np.max(ulp_diff_f32(Mg[:, s], momentum_ref_f32(M0[:, s], G0[:, s], hp))) <= 1
+        check_w(Wg[:, s], ref["W"], hp, ref["scale"], bf16=True)
+
+
+# ---------------------------------------------------------------------------
+# device status
+# ---------------------------------------------------------------------------
+def test_nonfinite_gradient_is_flagged():
+    W, G, M = workloads.random_case(50, 128, 256, batch=1)
+    G[0, 3, 5] = float("nan")
+    code, flags = step_once([m.Group.stacked(W.to(DEV), G.to(DEV), M.to(DEV))], {})
+    assert code == m.MUON_OK and (flags & m.MUON_FLAG_NONFINITE)
+
+
+def test_misaligned_pointer_in_device_array_is_flagged_and_skipped():
+    """A matrix whose pointer is not 16-byte aligned is detected by the kernel
+    before any access, flagged, and left untouched; the others are updated."""
+    W, G, M = workloads.random_case(51, 128, 256, batch=2)
+    Wd, Gd, Md = W.to(DEV), G.to(DEV), M.to(DEV)
+    grp = m.Group.stacked(Wd, Gd, Md)
+    grp.ptrs[1, 1] += 2                       # G of matrix 1 shifted by one bf16 element
+    W1, M1 = Wd[1].clone(), Md[1].clone()
+    code, flags = step_once([grp], {})
+    assert code == m.MUON_OK and (flags & m.MUON_FLAG_MISALIGNED)
+    assert torch.equal(Wd[1], W1) and torch.equal(Md[1], M1)
+    assert not torch.equal(Md[0], M[0].to(DEV))
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    ws = m.workspace(256)
+    m.muon_check_wait_timeout(ws, 2_000_000)           # 2 ms
+    code, flags = m.muon_get_status(ws)
+    assert code == m.MUON_ERR_TIMEOUT and (flags & m.MUON_FLAG_TIMEOUT)
+    x = torch.randn(1, 128, 256, device=DEV)
+    got = run_ns(x)
+    assert rel_fro(f64(got[0]), oracle.newton_schulz(f64(x[0]))) <= NS_TOL
