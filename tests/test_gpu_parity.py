@@ -91,7 +91,7 @@ def test_ns_without_normalisation_fixes_orthonormal_rows():
     (p(1) = 1, p'(1) = 0)."""
     rng = np.random.default_rng(3)
     Q, _ = np.linalg.qr(rng.standard_normal((512, 256)))
-    x = torch.tensor(Q.T[None], dtype=torch.float32).to(DEV)          # 256 x 512
+    x = torch.tensor(np.ascontiguousarray(Q.T[None]), dtype=torch.float32).to(DEV)  # 256 x 512
     sched = m.Schedule([(2, (2.0, -1.5, 0.5))], normalize=False)
     got = f64(run_ns(x, sched)[0])
     assert rel_fro(got, Q.T) <= 1e-2
