@@ -216,6 +216,34 @@ muon_status_t muon_set_wait_timeout_ns(uint64_t ns);
 muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
                                       uint64_t timeout_ns, muon_stream_t stream);
 
+/* Allocation-free variant of newton_schulz_batched.  The pages have no
+ * counterpart to it; it exists for callers that cannot obtain a workspace
+ * from cudaMalloc: code inside a framework whose caching allocator owns all
+ * device memory (a raw cudaMalloc there fragments memory and escapes the
+ * framework's accounting), and latency-critical loops that cannot pay the
+ * implicit device synchronisation cudaMalloc / cudaFree may cause.
+ *
+ * Same arguments and results as newton_schulz_batched, without the
+ * workspace: the scratch is a 32 MiB array inside the library's device image
+ * (held by every GPU the library is loaded on until the process exits).  A
+ * call whose workspace need (newton_schulz_workspace_size) exceeds 32 MiB
+ * returns MUON_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The
+ * call allocates no device memory.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current), so make that first
+ * call before any stream capture.  All calls share the one array and every
+ * call rewrites what it reads, so stale contents do not matter, but calls
+ * that may overlap on the GPU (different streams, several host threads)
+ * race on it and must be serialised by the caller.
+ *
+ * device_flags: NULL, or a caller-owned 4-byte-aligned device word that
+ * receives this call's MUON_FLAG_* bits (stream-ordered copy at the end). */
+muon_status_t newton_schulz_batched_noalloc(const void* x, muon_dtype_t xdt,
+                                            const muon_view_t* view, int batch, void* out,
+                                            muon_dtype_t odt, const muon_ns_schedule_t* schedule,
+                                            uint32_t* device_flags, muon_stream_t stream);
+
 /* Per-kernel statistics since the last muon_profile_reset.  Launches are
  * always counted.  With profiling on, the library records a CUDA event pair
  * on the launching stream around every kernel launch and total_ms sums their

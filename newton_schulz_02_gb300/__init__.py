@@ -91,6 +91,9 @@ PROTOTYPES = {
     "newton_schulz_batched": (c_int, [c_void_p, c_int, POINTER(muon_view_t), c_int, c_void_p,
                                       c_int, POINTER(muon_ns_schedule_t), c_void_p, c_size_t,
                                       c_void_p]),
+    "newton_schulz_batched_noalloc": (c_int, [c_void_p, c_int, POINTER(muon_view_t), c_int,
+                                              c_void_p, c_int, POINTER(muon_ns_schedule_t),
+                                              c_void_p, c_void_p]),
     "muon_get_status": (c_int, [c_void_p, c_void_p, POINTER(c_uint32)]),
     "muon_set_wait_timeout_ns": (c_int, [c_uint64]),
     "muon_check_wait_timeout": (c_int, [c_void_p, c_size_t, c_uint64, c_void_p]),
@@ -292,6 +295,24 @@ def newton_schulz_batched(x: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, 
                                                 int(batch), out.data_ptr(), _DT[out.dtype],
                                                 _sched_ref(schedule), ws.data_ptr(), ws.numel(),
                                                 _stream(stream)), "newton_schulz_batched")
+
+
+def newton_schulz_batched_noalloc(x: torch.Tensor, out: torch.Tensor, schedule=None,
+                                  device_flags: Optional[torch.Tensor] = None,
+                                  stream=None) -> int:
+    """newton_schulz_batched on the library's own static scratch (no
+    workspace argument, no device allocation).  For callers that cannot
+    allocate device memory themselves; see include/muon.h.  Returns the C
+    status code instead of raising, so callers can see a too-large request
+    (MUON_ERR_WORKSPACE_TOO_SMALL)."""
+    x3 = x if x.dim() == 3 else x.unsqueeze(0)
+    if x3.stride(2) != 1 or not out.is_contiguous():
+        raise ValueError("x needs unit column stride and out must be contiguous")
+    view = muon_view_t(x3.shape[1], x3.shape[2], x3.stride(1), x3.stride(0), 0)
+    flags_ptr = device_flags.data_ptr() if device_flags is not None else None
+    return load_library().newton_schulz_batched_noalloc(
+        x.data_ptr(), _DT[x.dtype], ctypes.byref(view), x3.shape[0], out.data_ptr(),
+        _DT[out.dtype], _sched_ref(schedule), flags_ptr, _stream(stream))
 
 
 def muon_get_status(ws: torch.Tensor, stream=None) -> tuple[int, int]:
