@@ -36,7 +36,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["stack", "single", "heads"], default="stack")
+    ap.add_argument("--workload", choices=["stack", "single", "heads", "dense", "moe"],
+                    default="stack")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -75,6 +76,38 @@ def build_workload(name: str, rank: int):
                 desc=dict(workload="heads: QKV 4096 x (32 x 128) bf16 split per head",
                           matrices=32, rows=4096, cols=128, w_dtype="bf16", g_dtype="bf16",
                           m_dtype="fp32", scale="spectral", seed=2))
+
+
+def device_sets(name: str, rank: int, dev):
+    """Multi-GB sets drawn on the device: {shape name: (W [B,r,c], G, M)}."""
+    import workloads
+    if name == "dense":
+        sets = workloads.dense_layers(seed=3 + 1000 * rank, device=dev)
+        desc = dict(workload="dense: 32 layers x {q,o 4096^2; k,v 1024x4096; gate,up 14336x4096; "
+                             "down 4096x14336}", matrices=32 * 7, w_dtype="bf16", g_dtype="bf16",
+                    m_dtype="fp32", scale="spectral", seed=3, grads="Gaussian 1e-3 + rank-8 spike")
+    else:
+        sets = workloads.moe_experts(seed=4 + 1000 * rank, device=dev)
+        desc = dict(workload="moe: 256 experts x {up 2048x7168, down 7168x2048}", matrices=512,
+                    w_dtype="bf16", g_dtype="bf16", m_dtype="fp32", scale="spectral", seed=4,
+                    grads="1e-3 * Student-t(3)")
+    return sets, desc
+
+
+def set_groups(m, sets):
+    """One group per shape (muon_group_by_shape), every matrix of the set."""
+    mats, descs = [], []
+    for nm, (W, G, M) in sets.items():
+        for b in range(W.shape[0]):
+            mats.append((nm, b))
+            descs.append((W.shape[1], W.shape[2], W.shape[2], m.MUON_BF16, m.MUON_BF16, 0))
+    gid, ng = m.muon_group_by_shape(descs, 0)
+    groups = []
+    for g in range(ng):
+        mem = [mats[i] for i in range(len(mats)) if gid[i] == g]
+        groups.append(m.Group([sets[nm][0][b] for nm, b in mem], [sets[nm][1][b] for nm, b in mem],
+                              [sets[nm][2][b] for nm, b in mem]))
+    return groups
 
 
 def make_groups(m, wl, Wd, Md, Gd):
@@ -169,6 +202,24 @@ def oracle_sample(wl, seconds: float, min_units: int = 1):
     return params / dt, done, dt
 
 
+def oracle_sample_sets(sets, seconds: float):
+    """Oracle on matrices of a device-drawn set (copied to the host one by one),
+    smallest shape first, until `seconds` have passed (at least one matrix)."""
+    import numpy as np
+    import oracle
+    hp = oracle.MuonHyper()
+    order = sorted(sets.items(), key=lambda kv: kv[1][0].shape[1] * kv[1][0].shape[2])
+    nm, (W, G, M) = order[0]
+    done, params, t0 = 0, 0, time.perf_counter()
+    while done < 1 or (time.perf_counter() - t0 < seconds and done < W.shape[0]):
+        oracle.muon_step(W[done].float().cpu().numpy().astype(np.float64),
+                         G[done].float().cpu().numpy().astype(np.float64),
+                         M[done].cpu().numpy().astype(np.float64), hp)
+        params += W[done].numel()
+        done += 1
+    return params / (time.perf_counter() - t0), done, time.perf_counter() - t0, W.shape[1], W.shape[2]
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -182,6 +233,22 @@ def dist_setup(args):
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest `value` over all ranks (a no-op for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(steps: int, params_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job params/s: every rank updates params_per_rank per step."""
+    return world * steps * params_per_rank / (ms_max / 1e3)
 
 
 def run_reference(args):
@@ -252,14 +319,20 @@ def run_ours(args):
     m.load_library()
     peaks, peak_src = load_peaks()
 
-    wl = build_workload(args.workload, rank)
-    Wd = wl["W"].to(dev)
-    Md = wl["M"].to(dev)
-    Gd = [g.to(dev) for g in wl["grads"]]
-    groups = make_groups(m, wl, Wd, Md, Gd)
+    if args.workload in ("dense", "moe"):
+        sets, desc = device_sets(args.workload, rank, dev)
+        groups = [set_groups(m, sets)]
+        P = int(sum(W.numel() for W, _, _ in sets.values()))
+        wl = {"kind": args.workload, "sets": sets, "desc": desc}
+    else:
+        wl = build_workload(args.workload, rank)
+        Wd = wl["W"].to(dev)
+        Md = wl["M"].to(dev)
+        Gd = [g.to(dev) for g in wl["grads"]]
+        groups = make_groups(m, wl, Wd, Md, Gd)
+        P = n_params(wl)
     hp = m.hparams()
     ws = m.workspace(m.muon_step_workspace_size(groups[0]), device=dev)
-    P = n_params(wl)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -290,11 +363,8 @@ def run_ours(args):
     code, flags = m.muon_get_status(ws)
     if code != m.MUON_OK or flags:
         raise RuntimeError(f"device status {code} flags {flags:#x} after timed steps")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * args.steps * P / (ms / 1e3)
+    ms = max_over_ranks(ms, world, dev)
+    value = job_value(args.steps, P, world, ms)
 
     # ---- per-kernel roofline (event-timed on the launching stream) --------
     gemm = {k: prof[k] for k in ("ns_gram", "ns_poly", "ns_update") if prof[k]["launches"]}
@@ -335,7 +405,10 @@ def run_ours(args):
 
     # ---- end to end: host buffers, copies inside the timed region ------------
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.workload in ("dense", "moe"):
+        e2e = {"value": None, "unit": "params/s", "skipped": "multi-GB device-drawn set; the "
+               "end-to-end leg runs on the stacked workload"}
+    elif args.e2e_steps > 0:
         Gh = [g.pin_memory() for g in wl["grads"]]
         Gslot = torch.empty_like(Gd[0])
         Wh = torch.empty(Wd.shape, dtype=Wd.dtype).pin_memory()
@@ -358,14 +431,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
         if any(c != m.MUON_OK or f for c, f in flags_h):
             raise RuntimeError("device status set during the end-to-end steps")
-        e2e = {"value": world * args.e2e_steps * P / (e_ms / 1e3), "unit": "params/s",
+        e2e = {"value": job_value(args.e2e_steps, P, world, e_ms), "unit": "params/s",
                "h2d_bytes_per_step": int(Gslot.numel() * Gslot.element_size()),
                "d2h_bytes_per_step": int(Wh.numel() * Wh.element_size() + 4),
                "steps": args.e2e_steps, "wall_s": round(wall, 4),
@@ -377,13 +446,19 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    cpu_v, cpu_n, cpu_dt = oracle_sample(wl, args.cpu_seconds)
-    rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
+    if "sets" in wl:
+        cpu_v, cpu_n, cpu_dt, rows, cols = oracle_sample_sets(wl["sets"], args.cpu_seconds)
+    else:
+        cpu_v, cpu_n, cpu_dt = oracle_sample(wl, args.cpu_seconds)
+        rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
     clocks = clk.summary()
     desc = dict(wl["desc"])
     desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
-                l2="inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M + 512 MiB workspace"
-                if wl["kind"] == "stack" else "small workload (L2-resident)")
+                l2={"stack": "inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M "
+                             "+ 768 MiB workspace",
+                    "dense": "inputs larger than L2 (about 56 GB of W, G, M)",
+                    "moe": "inputs larger than L2 (about 60 GB of W, G, M)"}.get(
+                    wl["kind"], "small workload (L2-resident between steps)"))
     out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",

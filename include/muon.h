@@ -82,8 +82,10 @@ typedef enum {
   MUON_SCALE_NONE = 2
 } muon_scale_mode_t;
 
-/* Precision of the Newton–Schulz chain: bf16 operands with fp32 accumulation
- * and fp32 epilogues.  MUON_NS_TF32 is reserved (returns MUON_ERR_UNSUPPORTED). */
+/* Precision of the Newton–Schulz chain: bf16 tensor-core operands with fp32
+ * accumulation and fp32 epilogues; X X^T and the polynomial are stored in
+ * bf16, the iterate as a bf16 value plus its bf16 rounding residual (about 16
+ * significant bits).  MUON_NS_TF32 is reserved (returns MUON_ERR_UNSUPPORTED). */
 typedef enum { MUON_NS_BF16 = 0, MUON_NS_TF32 = 1 } muon_ns_precision_t;
 
 /* `steps` iterations of X <- a X + b (X X^T) X + c (X X^T)^2 X. */
@@ -190,8 +192,8 @@ muon_status_t newton_schulz_workspace_size(const muon_view_t* view, int batch,
  * x: device, matrix i at x + i*view->batch_stride elements, dtype xdt, view.
  * out: device, dense [batch, rows, cols] row-major of dtype odt (written, in
  * the input's orientation).  x and out must not overlap.  The chain runs in
- * the precision schedule->prec names; its last iterate is bf16, widened for
- * odt = MUON_F32. */
+ * the precision schedule->prec names; the last iterate (value + residual) is
+ * rounded to odt. */
 muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_view_t* view,
                                     int batch, void* out, muon_dtype_t odt,
                                     const muon_ns_schedule_t* schedule, void* workspace,

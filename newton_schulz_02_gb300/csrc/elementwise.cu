@@ -2,10 +2,11 @@
 //
 //  * k_prepare_*: momentum M_t = mu*M + G and look-ahead X = mu*M_t + G
 //    ("Muon 优化器" Algorithm 1; the 'ema' variant of "RFC-0023" §方案 1), or a
-//    plain load for newton_schulz_batched; writes X as bf16 into the
-//    workspace in the wide orientation (transposing tall matrices through
-//    shared memory) with zero padding, and per-block partial sums of X^2 for
-//    the Frobenius norm of "Muon 优化器" §2.  16-byte vector accesses.
+//    plain load for newton_schulz_batched; writes X as two bf16 planes
+//    (hi, and lo = the rounding residual) into the workspace in the wide
+//    orientation (transposing tall matrices through shared memory) with zero
+//    padding, and per-block partial sums of X^2 for the Frobenius norm of
+//    "Muon 优化器" §2.  16-byte vector accesses.
 //  * k_finalize_norm: deterministic per-matrix sum of the partials -> 1/||X||_F.
 //  * k_apply_*: W <- W*(1 - lr*wd*mask) - lr*scale*O' (Algorithm 1), or a
 //    plain store of O' for newton_schulz_batched.
@@ -63,12 +64,16 @@ __device__ __forceinline__ void store8(void* base, int64_t off, int dtype, const
   }
 }
 
-__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
-  uint4 u;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+// hi = bf16(v), lo = bf16(v - hi): v to about 16 significant bits.
+__device__ __forceinline__ void split_bf16x8(const float (&v)[8], uint4& hi, uint4& lo) {
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&hi);
+  __nv_bfloat162* l = reinterpret_cast<__nv_bfloat162*>(&lo);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
-  return u;
+  for (int k = 0; k < 4; ++k) {
+    h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+    const float2 f = __bfloat1622float2(h[k]);
+    l[k] = __floats2bfloat162_rn(v[2 * k] - f.x, v[2 * k + 1] - f.y);
+  }
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float (&v)[8]) {
@@ -174,7 +179,11 @@ __global__ void __launch_bounds__(kThreads) k_prepare_wide(PrepareArgs p) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) x[k] = 0.f;
     }
-    *reinterpret_cast<uint4*>(X + static_cast<int64_t>(i) * p.m_pad + j) = pack_bf16x8(x);
+    uint4 hi, lo;
+    split_bf16x8(x, hi, lo);
+    const int64_t o = static_cast<int64_t>(i) * p.m_pad + j;
+    *reinterpret_cast<uint4*>(X + o) = hi;
+    *reinterpret_cast<uint4*>(X + p.x_lo_off + o) = lo;
   }
   const float s = block_sum(acc, red);
   if (threadIdx.x == 0) p.partials[static_cast<int64_t>(b) * p.parts + blockIdx.x] = s;
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(kThreads) k_prepare_wide(PrepareArgs p) {
 // ---- pass 1, tall (rows > cols): X_ws[j][i] = X[i][j] via 64x64 smem tiles ---
 __global__ void __launch_bounds__(kThreads) k_prepare_tall(PrepareArgs p) {
   __shared__ float red[kThreads / 32];
-  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTile + 8];
+  __shared__ float tile[kTile][kTile + 1];
   const int b = blockIdx.y;
   const MatrixPtrs mp = matrix_ptrs(p, b);
   if (mp.skip && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -211,18 +220,22 @@ __global__ void __launch_bounds__(kThreads) k_prepare_tall(PrepareArgs p) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = 0.f;
       }
-      *reinterpret_cast<uint4*>(&tile[r][c8]) = pack_bf16x8(x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[r][c8 + e] = x[e];
     }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int q = threadIdx.x + k * kThreads;
       const int jj = q >> 3, ii8 = (q & 7) * 8;
-      uint4 u;
-      __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(&u);
+      float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = tile[ii8 + e][jj];
-      *reinterpret_cast<uint4*>(X + static_cast<int64_t>(j0 + jj) * p.m_pad + i0 + ii8) = u;
+      for (int e = 0; e < 8; ++e) v[e] = tile[ii8 + e][jj];
+      uint4 hi, lo;
+      split_bf16x8(v, hi, lo);
+      const int64_t o = static_cast<int64_t>(j0 + jj) * p.m_pad + i0 + ii8;
+      *reinterpret_cast<uint4*>(X + o) = hi;
+      *reinterpret_cast<uint4*>(X + p.x_lo_off + o) = lo;
     }
     __syncthreads();
   }
@@ -285,15 +298,21 @@ __global__ void __launch_bounds__(kThreads) k_apply_wide(ApplyArgs p) {
        v += static_cast<int64_t>(gridDim.x) * kThreads) {
     const int i = static_cast<int>(v / vpr);
     const int j = static_cast<int>(v - static_cast<int64_t>(i) * vpr) * 8;
-    float o[8];
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(X + static_cast<int64_t>(i) * p.m_pad + j), o);
+    const int64_t xo = static_cast<int64_t>(i) * p.m_pad + j;
+    float o[8], ol[8];
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(X + xo), o);
+    if (p.has_lo) {
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(X + p.x_lo_off + xo), ol);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] += ol[e];
+    }
     apply8(p, b, wbase, static_cast<int64_t>(i) * ld + j, o);
   }
 }
 
 // ---- last pass, tall: W[i][j] from X_ws[j][i] ----------------------------------------
 __global__ void __launch_bounds__(kThreads) k_apply_tall(ApplyArgs p) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTile + 8];
+  __shared__ float tile[kTile][kTile + 1];
   const int b = blockIdx.y;
   if (p.skip[b]) return;
   void* wbase = apply_base(p, b);
@@ -308,8 +327,12 @@ __global__ void __launch_bounds__(kThreads) k_apply_tall(ApplyArgs p) {
     for (int k = 0; k < 2; ++k) {
       const int q = threadIdx.x + k * kThreads;
       const int jj = q >> 3, ii8 = (q & 7) * 8;
-      *reinterpret_cast<uint4*>(&tile[jj][ii8]) =
-          *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(j0 + jj) * p.m_pad + i0 + ii8);
+      const int64_t xo = static_cast<int64_t>(j0 + jj) * p.m_pad + i0 + ii8;
+      float v[8], vl[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      unpack_bf16x8(*reinterpret_cast<const uint4*>(X + xo), v);
+      if (p.has_lo) unpack_bf16x8(*reinterpret_cast<const uint4*>(X + p.x_lo_off + xo), vl);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tile[jj][ii8 + e] = v[e] + vl[e];
     }
     __syncthreads();
 #pragma unroll
@@ -320,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) k_apply_tall(ApplyArgs p) {
       if (i < p.rows && j < p.cols) {
         float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = __bfloat162float(tile[c8 + e][r]);
+        for (int e = 0; e < 8; ++e) o[e] = tile[c8 + e][r];
         apply8(p, b, wbase, static_cast<int64_t>(i) * ld + j, o);
       }
     }
@@ -366,9 +389,9 @@ int apply_parts(int rows, int cols) {
 
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st) {
   dim3 grid(a.parts, a.batch);
-  // algorithmic bytes: read G, read + write M (momentum modes), write bf16 X
+  // algorithmic bytes: read G, read + write M (momentum modes), write X (hi + lo planes)
   const double elems = static_cast<double>(a.batch) * a.rows * a.cols;
-  const double per = (a.g_dtype == MUON_BF16 ? 2.0 : 4.0) + (a.mode == kPrepLoad ? 0.0 : 8.0) + 2.0;
+  const double per = (a.g_dtype == MUON_BF16 ? 2.0 : 4.0) + (a.mode == kPrepLoad ? 0.0 : 8.0) + 4.0;
   prof_begin(kKindPrepare, st);
   if (a.tall)
     k_prepare_tall<<<grid, kThreads, 0, st>>>(a);
@@ -387,10 +410,10 @@ cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st) {
 
 cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st) {
   dim3 grid(a.parts, a.batch);
-  // algorithmic bytes: read bf16 O'; read + write W (mode 0) or write out (mode 1)
+  // algorithmic bytes: read O' (hi, and lo when present); read + write W (mode 0) or write out
   const double elems = static_cast<double>(a.batch) * a.rows * a.cols;
   const double wsz = a.w_dtype == MUON_BF16 ? 2.0 : 4.0;
-  const double per = 2.0 + (a.mode == 0 ? 2.0 * wsz : wsz);
+  const double per = (a.has_lo ? 4.0 : 2.0) + (a.mode == 0 ? 2.0 * wsz : wsz);
   prof_begin(kKindApply, st);
   if (a.tall)
     k_apply_tall<<<grid, kThreads, 0, st>>>(a);

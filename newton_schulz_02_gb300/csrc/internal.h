@@ -25,9 +25,14 @@ inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 enum PrepMode : int { kPrepMomentumSgd = 0, kPrepMomentumEma = 1, kPrepLoad = 2 };
 
-// Pass 1: momentum (+ look-ahead) or a plain load, writing the bf16 iterate
-// X into the workspace (wide orientation, padded) and per-block partial sums
-// of X^2 (fp32, from the fp32 value before the bf16 cast).
+// The Newton–Schulz iterate is kept as two bf16 planes, X = hi + lo, with
+// lo = bf16(x - hi) the rounding residual: the tensor cores read hi only,
+// while the a*X term of every update uses hi + lo (about 16 significant
+// bits).  The lo plane of an iterate sits lo_off elements after its hi plane.
+//
+// Pass 1: momentum (+ look-ahead) or a plain load, writing the iterate X
+// (hi and lo planes) into the workspace (wide orientation, padded) and
+// per-block partial sums of X^2 (fp32, from the fp32 value before rounding).
 struct PrepareArgs {
   int batch, rows, cols;
   int64_t row_stride;    // elements, of G, M and W
@@ -42,7 +47,8 @@ struct PrepareArgs {
   float mu;            // sgd: mu; ema: beta
   double ema_omb;      // ema: 1 - beta (exact, from the fp32 beta)
   float c_mom, c_grad;  // ema look-ahead: X = c_mom*buf + c_grad*g
-  __nv_bfloat16* X;     // [batch][n_pad][m_pad]
+  __nv_bfloat16* X;     // hi plane [batch][n_pad][m_pad]; lo plane at X + x_lo_off
+  int64_t x_lo_off;
   int n_pad, m_pad;
   int tall;             // rows > cols: X holds the transpose
   int parts;            // blocks per matrix (partials per matrix)
@@ -71,7 +77,9 @@ struct ApplyArgs {
   const uint8_t* wd_mask;    // mode 0, may be nullptr
   float decay_on;            // 1 - lr*wd
   float lr_scale;            // lr * scale
-  const __nv_bfloat16* X;    // final iterate [batch][n_pad][m_pad]
+  const __nv_bfloat16* X;    // final iterate, hi plane [batch][n_pad][m_pad]
+  int64_t x_lo_off;          // lo plane at X + x_lo_off
+  int has_lo;                // 0: the final iterate is the hi plane alone
   int n_pad, m_pad, tall;
   int parts;
   const uint8_t* skip;
@@ -81,10 +89,12 @@ struct ApplyArgs {
 struct NsChainArgs {
   int batch, n_pad, m_pad;
   int n, m;             // unpadded sizes (algorithmic flop counts)
-  __nv_bfloat16* X0;
+  __nv_bfloat16* X0;    // hi planes; lo planes at X0 + lo_off, X1 + lo_off
   __nv_bfloat16* X1;
+  int64_t lo_off;
   __nv_bfloat16* A;
   __nv_bfloat16* B;
+  float* pdiag;         // [batch][n_pad] fp32 residual of P's diagonal
   const float* inv_s;   // folded into the first iteration; nullptr = no normalisation
   const float* coeffs;  // host [iters][3]
   int iters;
@@ -113,6 +123,9 @@ cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st);
 cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st);
 cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
+
+// Whether the chain's last iterate (after `iters` iterations) carries a lo plane.
+bool ns_final_has_lo(int iters);
 
 // Runs the whole chain; the final iterate is left in X0 if the number of
 // iterations is even, else in X1.  Returns cudaErrorNotSupported when the

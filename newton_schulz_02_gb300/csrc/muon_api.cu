@@ -43,7 +43,8 @@ int dsize(int d) { return d == MUON_BF16 ? 2 : 4; }
 
 struct Layout {
   int n_pad = 0, m_pad = 0, parts = 0;
-  size_t x0 = 0, x1 = 0, a = 0, b = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
+  int64_t lo_off = 0;  // elements from an iterate's hi plane to its lo plane
+  size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
 };
 
 Layout layout_for(int batch, int rows, int cols) {
@@ -54,11 +55,14 @@ Layout layout_for(int batch, int rows, int cols) {
   L.parts = prepare_parts(rows, cols, L.n_pad, L.m_pad);
   const size_t xb = static_cast<size_t>(batch) * L.n_pad * L.m_pad * 2;
   const size_t sb = static_cast<size_t>(batch) * L.n_pad * L.n_pad * 2;
+  L.lo_off = static_cast<int64_t>(align256(xb) / 2);
   size_t off = kHeaderBytes;
-  L.x0 = off; off += align256(xb);
-  L.x1 = off; off += align256(xb);
+  // each iterate: hi plane, then lo plane (lo_off = batch*n_pad*m_pad elements)
+  L.x0 = off; off += 2 * align256(xb);
+  L.x1 = off; off += 2 * align256(xb);
   L.a = off; off += align256(sb);
   L.b = off; off += align256(sb);
+  L.pdiag = off; off += align256(static_cast<size_t>(batch) * L.n_pad * 4);
   L.partials = off; off += align256(static_cast<size_t>(batch) * L.parts * 4);
   L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
   L.skip = off; off += align256(static_cast<size_t>(batch));
@@ -144,8 +148,10 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   na.m = v.rows < v.cols ? v.cols : v.rows;
   na.X0 = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
   na.X1 = reinterpret_cast<__nv_bfloat16*>(ws + L.x1);
+  na.lo_off = L.lo_off;
   na.A = reinterpret_cast<__nv_bfloat16*>(ws + L.a);
   na.B = reinterpret_cast<__nv_bfloat16*>(ws + L.b);
+  na.pdiag = reinterpret_cast<float*>(ws + L.pdiag);
   na.inv_s = normalize ? reinterpret_cast<const float*>(ws + L.inv_s) : nullptr;
   na.coeffs = coeffs.data();
   na.iters = iters;
@@ -156,6 +162,8 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   if (e != cudaSuccess) return MUON_ERR_CUDA;
 
   ap.X = (iters % 2 == 0) ? na.X0 : na.X1;
+  ap.x_lo_off = L.lo_off;
+  ap.has_lo = ns_final_has_lo(iters) ? 1 : 0;
   ap.n_pad = L.n_pad;
   ap.m_pad = L.m_pad;
   ap.tall = v.rows > v.cols;
@@ -307,6 +315,7 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
     pa.c_mom = static_cast<float>(c_mom);
     pa.c_grad = static_cast<float>(c_grad);
     pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
+    pa.x_lo_off = L.lo_off;
     pa.n_pad = L.n_pad;
     pa.m_pad = L.m_pad;
     pa.tall = g.view.rows > g.view.cols;
@@ -392,6 +401,7 @@ muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_
   pa.g_base = x;
   pa.mode = kPrepLoad;
   pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
+  pa.x_lo_off = L.lo_off;
   pa.n_pad = L.n_pad;
   pa.m_pad = L.m_pad;
   pa.tall = view->rows > view->cols;

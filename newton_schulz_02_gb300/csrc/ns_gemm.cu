@@ -2,16 +2,19 @@
 //
 // One iteration of "Muon 优化器" (DeepSeek-V4 tech notes) §2,
 //     X <- a X + b (X X^T) X + c (X X^T)^2 X,
-// runs as three batched GEMMs on the wide, zero-padded bf16 iterate X (n x m):
+// runs as three batched GEMMs on the wide, zero-padded iterate X (n x m):
 //
-//   Gram    S = X X^T            n x n, K = m  (symmetric: upper tiles + mirror)
-//   Poly    P = b S + c S S      n x n, K = n  (symmetric: upper tiles + mirror)
-//   Update  X' = a X + P X       n x m, K = n
+//   Gram    S = X X^T                      n x n, K = m  (symmetric: upper tiles + mirror)
+//   Poly    P = b S + c S S + (a - 1) I    n x n, K = n  (symmetric: upper tiles + mirror)
+//   Update  X' = X + P X                   n x m, K = n
 //
-// so that  a X + b S X + c S^2 X = a X + (b S + c S^2) X.  When c == 0 the
-// Poly GEMM is skipped and the Update uses S with weight b.  The Frobenius
-// normalisation is folded into the first iteration: with s = ||X||_F,
-// S_0 = (X X^T)/s^2 and X_1 = (a X + P_0 X)/s.
+// which is  a X + b S X + c S^2 X  exactly.  When c == 0 the Gram epilogue
+// writes P = b S + (a - 1) I directly and the Poly GEMM is skipped.  P is
+// stored in bf16 except for the rounding residual of its diagonal, kept in
+// fp32 and added back in the update (the shifted diagonal is large and its
+// bf16 rounding would otherwise swamp b S_ii when a is small).  The
+// Frobenius normalisation is folded into the first iteration: with
+// s = ||X||_F, S_0 = (X X^T)/s^2 and X_1 = (X + P_0 X)/s.
 //
 // Kernel shape (one persistent CTA per SM, 6 warps):
 //   warp 0      one thread issues TMA loads of A and B k-blocks into a
@@ -19,10 +22,28 @@
 //   warp 1      allocates TMEM and one thread issues tcgen05.mma
 //               (M=128, N=BN, K=16, bf16 -> fp32) into one of two TMEM
 //               accumulators, committing to mbarriers;
-//   warps 2-5   epilogue: tcgen05.ld of their 32 TMEM lanes, fp32 epilogue
-//               math, bf16 stores (and the mirrored store of symmetric tiles).
+//   warps 2-5   epilogue (one per 32-lane TMEM quarter): tcgen05.ld, fp32
+//               epilogue math, bf16 stores (and the mirrored store of
+//               off-diagonal symmetric tiles).
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
-// All operands are bf16 with fp32 accumulation; outputs are rounded to bf16.
+//
+// Precision.  Operands are bf16 with fp32 accumulation; S and P are stored
+// as bf16; the iterate is stored as two bf16 planes X = hi + lo with
+// lo = bf16(x - hi) for the first kLoIters iterations and as hi alone after
+// that.  The exact X term of the update reads hi + lo.  In the first
+// kResidualIters iterations the product also reads both planes (P hi + P lo,
+// one K-loop over the two planes); later iterations read hi.
+// Why: when a few singular directions dominate the entries (a low-rank
+// spike in the gradient), rounding X to bf16 puts noise the size of the
+// large entries into the small directions, which the fast stage multiplies
+// by a ~ 3.4 per step, so both the X term and, while those directions are
+// still small, the product need the residual.  Writing the update as
+// X + P X with the a - 1 shift inside P keeps the product's coefficient small
+// on directions that have converged (a + b + c - 1: -0.30 in the fast stage,
+// 0 in the stable stage), so dropping lo from the product in later
+// iterations costs little; written as a X + (b S + c S^2) X, converged
+// directions would cancel 3.44 X against -2.74 X and amplify the dropped
+// residual about ninefold.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,8 +60,11 @@ namespace muon {
 namespace {
 
 constexpr int kBM = 128;  // tile rows (TMEM lanes)
+constexpr int kResidualIters = 2;  // iterations whose product also reads the lo plane
+constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 4;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
 
 enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2 };
 
@@ -61,7 +85,14 @@ struct GemmParams {
   int64_t out_ld, out_bstride;
   const __nv_bfloat16* aux;
   int64_t aux_ld, aux_bstride;
+  int64_t lo_off;  // update: lo planes of aux and out at +lo_off elements
+  int lo_in, lo_out;  // update: read aux's lo plane / write out's lo plane
   float ca, cb, cc;
+  float cd;         // added on the diagonal (Gram when c == 0, Poly): a - 1
+  int kplanes;      // update: 1 = B from hi; 2 = K-loop over hi then lo (tmB2)
+  float* pdiag;     // Gram (c == 0) / Poly: fp32 rounding residual of P's diagonal, [batch][n]
+  const float* pdiag_in;  // update: that residual, added back as d_row * X
+  int64_t pdiag_bstride;
   const float* mscale;
   uint32_t* status;
   uint64_t timeout_ns;
@@ -104,12 +135,16 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
+__device__ __forceinline__ void load_raw4(const __nv_bfloat16* src, uint4 (&u)[4]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
 #pragma unroll
+  for (int q = 0; q < 4; ++q) u[q] = s[q];
+}
+
+__device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32]) {
+#pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = s[q];
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[q]);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float2 f = __bfloat1622float2(h[k]);
@@ -122,7 +157,7 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v
 template <int BN, bool B_MN, int EPI, bool SYM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const GemmParams p) {
+              const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, B_MN);
@@ -149,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4 * 32);
+      mbar_init(&tempty[a], kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -157,6 +192,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.kplanes > 1) tma_prefetch_desc(&tmB2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -167,6 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nkb = p.K / kBK;
+  const int nkb_total = nkb * p.kplanes;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -177,20 +214,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
         int b, tm, tn;
         decode_tile<BN, SYM>(p, t, b, tm, tn);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb_total; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
+          const bool second = kb >= nkb;           // second plane of the B operand
+          const int k0 = (second ? kb - nkb : kb) * kBK;
+          const CUtensorMap* tb = second ? &tmB2 : &tmB;
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          tma_load_3d(smA + stage * C::kABytes, &tmA, &full[stage], kb * kBK, tm * kBM, b);
+          tma_load_3d(smA + stage * C::kABytes, &tmA, &full[stage], k0, tm * kBM, b);
           if (!B_MN) {
-            tma_load_3d(smB + stage * C::kBBytes, &tmB, &full[stage], kb * kBK, tn * BN, b);
+            tma_load_3d(smB + stage * C::kBBytes, tb, &full[stage], k0, tn * BN, b);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(smB + stage * C::kBBytes + j * (64 * kBK * 2), &tmB, &full[stage],
-                          tn * BN + j * 64, kb * kBK, b);
+              tma_load_3d(smB + stage * C::kBBytes + j * (64 * kBK * 2), tb, &full[stage],
+                          tn * BN + j * 64, k0, b);
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -215,7 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = 0; kb < nkb_total; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -256,59 +296,122 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter accessible to this warp
+    // Warps 2..5, one per TMEM lane quarter (warp & 3).  The residual operand
+    // of the next 32-column chunk is loaded while the current chunk is
+    // finished.  (Staging the mirrored store through shared memory was
+    // slower: it competes with the tensor core for shared-memory bandwidth.)
+    constexpr int kChunks = BN / 32;
+    constexpr int kChunksPerWarp = kChunks / (kEpiWarps / 4);
+    const int q = warp & 3;
+    const int ep = warp - 2;
+    const int c_begin = (ep >> 2) * kChunksPerWarp;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       int b, tm, tn;
       decode_tile<BN, SYM>(p, t, b, tm, tn);
+      const int row0 = tm * kBM + q * 32;
+      const int row = row0 + lane;
+      const bool mirror = SYM && (tn > tm / (BN / kBM));
+      const __nv_bfloat16* aux_row =
+          (EPI == kEpiGram) ? nullptr
+                            : p.aux + static_cast<int64_t>(b) * p.aux_bstride +
+                                  static_cast<int64_t>(row) * p.aux_ld + tn * BN;
+      uint4 cur_h[4], cur_l[4], nxt_h[4], nxt_l[4];
+      const bool lo_in = (EPI == kEpiUpdate) && p.lo_in;
+      const bool lo_out = (EPI == kEpiUpdate) && p.lo_out;
+      if (EPI != kEpiGram) {
+        load_raw4(aux_row + c_begin * 32, cur_h);
+        if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
+      }
       if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, p.timeout_ns)) break;
       tc_fence_after();
-      const int row = tm * kBM + q * 32 + lane;
-      const bool mirror = SYM && (tn > tm / (BN / kBM));
       float ms = 1.f;
       if (p.mscale != nullptr) ms = p.mscale[b];
       __nv_bfloat16* out = p.out + static_cast<int64_t>(b) * p.out_bstride;
-      const __nv_bfloat16* aux =
-          (EPI == kEpiGram) ? nullptr : p.aux + static_cast<int64_t>(b) * p.aux_bstride;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int i = 0; i < kChunksPerWarp; ++i) {
+        const int c = c_begin + i;
+        if (EPI != kEpiGram && i + 1 < kChunksPerWarp) {
+          load_raw4(aux_row + (c + 1) * 32, nxt_h);
+          if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait(r);
         const int col0 = tn * BN + c * 32;
         float v[32];
         if (EPI == kEpiGram) {
-          const float s2 = ms * ms;
+          const float s2 = ms * ms * p.cb;
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s2;
         } else {
           float x[32];
-          load_bf16x32(aux + static_cast<int64_t>(row) * p.aux_ld + col0, x);
+          unpack_raw4(cur_h, x);
           if (EPI == kEpiPoly) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cc, __uint_as_float(r[e]), p.cb * x[e]);
           } else {
+            float xl[32];
+            if (lo_in) {
+              unpack_raw4(cur_l, xl);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              v[e] = fmaf(p.cb, __uint_as_float(r[e]), p.ca * x[e]) * ms;
+              for (int e = 0; e < 32; ++e) xl[e] = 0.f;
+            }
+            const float d = p.pdiag_in[static_cast<int64_t>(b) * p.pdiag_bstride + row];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float xe = x[e] + xl[e];
+              v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
+            }
           }
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * p.out_ld + col0);
+        if (EPI != kEpiUpdate && p.pdiag != nullptr && row >= col0 && row < col0 + 32) {
+          // the (a - 1) I shift; the diagonal's bf16 rounding residual is kept
+          // in fp32 so that P's diagonal is exact to fp32 in the update
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (col0 + e == row) {
+              v[e] += p.cd;
+              p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
+                  v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+            }
+        }
+        __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
+        uint4* dst = reinterpret_cast<uint4*>(drow);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint4 u;
+          uint4 u, ul;
           __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+          __nv_bfloat162* hl = reinterpret_cast<__nv_bfloat162*>(&ul);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+          for (int e = 0; e < 4; ++e) {
+            const float v0 = v[8 * k + 2 * e], v1 = v[8 * k + 2 * e + 1];
+            h[e] = __floats2bfloat162_rn(v0, v1);
+            if (lo_out) {
+              const float2 f = __bfloat1622float2(h[e]);
+              hl[e] = __floats2bfloat162_rn(v0 - f.x, v1 - f.y);
+            }
+          }
           dst[k] = u;
+          if (lo_out) reinterpret_cast<uint4*>(drow + p.lo_off)[k] = ul;
         }
         if (mirror) {
+          // transposed copy: for each column e the warp's 32 lanes (32
+          // consecutive rows) store 64 contiguous bytes of row col0 + e
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = __float2bfloat16_rn(v[e]);
+        }
+        if (EPI != kEpiGram) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            cur_h[k] = nxt_h[k];
+            if (lo_in) cur_l[k] = nxt_l[k];
+          }
         }
       }
       tc_fence_before();
@@ -381,8 +484,8 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int batch, int K, int N) {
 }
 
 template <int BN, bool B_MN, int EPI, bool SYM>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                        double alg_flops, cudaStream_t st) {
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                        const GemmParams& p, double alg_flops, cudaStream_t st) {
   auto kern = k_ns_gemm<BN, B_MN, EPI, SYM>;
   const size_t smem = Cfg<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -391,16 +494,18 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   const int grid = std::max(1, std::min(p.total_tiles, sm_count()));
   const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
   prof_begin(kind, st);
-  kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, p);
+  kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);
   return cudaGetLastError();
 }
 
 struct OperandMaps {
-  CUtensorMap k128, kbn, mn;
+  CUtensorMap k128, kbn, mn, mn_lo;
 };
 
 }  // namespace
+
+bool ns_final_has_lo(int iters) { return iters < kLoIters; }
 
 cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   if (a.iters == 0) return cudaSuccess;
@@ -414,7 +519,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   for (int i = 0; i < 2; ++i) {
     if (!map_kmajor(&X[i].k128, xb[i], batch, n, m, kBM) ||
         !map_kmajor(&X[i].kbn, xb[i], batch, n, m, bn_sq) ||
-        !map_mnmajor(&X[i].mn, xb[i], batch, n, m))
+        !map_mnmajor(&X[i].mn, xb[i], batch, n, m) ||
+        !map_mnmajor(&X[i].mn_lo, xb[i] + a.lo_off, batch, n, m))
       return cudaErrorInvalidValue;
   }
   if (!map_kmajor(&S.k128, a.A, batch, n, n, kBM) || !map_kmajor(&S.kbn, a.A, batch, n, n, bn_sq) ||
@@ -440,11 +546,18 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.M = n; g.N = n; g.K = m;
     g.tiles_m = tm_sq; g.tiles_n = S_sq; g.tiles_per_matrix = sym_tiles;
     g.total_tiles = sym_tiles * batch;
-    g.out = a.A; g.out_ld = n; g.out_bstride = static_cast<int64_t>(n) * n;
+    g.out = (cc != 0.f) ? a.A : a.B;   // c == 0: the Gram epilogue writes P directly
+    g.out_ld = n; g.out_bstride = static_cast<int64_t>(n) * n;
+    g.cb = (cc != 0.f) ? 1.f : cb;
+    g.cd = (cc != 0.f) ? 0.f : ca - 1.f;
+    g.pdiag = (cc != 0.f) ? nullptr : a.pdiag;
+    g.pdiag_bstride = n;
+    g.kplanes = 1;
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    e = (bn_sq == 256) ? launch_gemm<256, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, g, f_gram, st)
-                       : launch_gemm<128, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, g, f_gram, st);
+    e = (bn_sq == 256)
+            ? launch_gemm<256, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st)
+            : launch_gemm<128, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
     if (e != cudaSuccess) return e;
 
     if (cc != 0.f) {
@@ -452,10 +565,11 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.K = n;
       q.out = a.B;
       q.aux = a.A; q.aux_ld = n; q.aux_bstride = static_cast<int64_t>(n) * n;
-      q.cb = cb; q.cc = cc;
+      q.cb = cb; q.cc = cc; q.cd = ca - 1.f;
+      q.pdiag = a.pdiag;
       q.mscale = nullptr;
-      e = (bn_sq == 256) ? launch_gemm<256, false, kEpiPoly, true>(S.k128, S.kbn, q, f_poly, st)
-                         : launch_gemm<128, false, kEpiPoly, true>(S.k128, S.kbn, q, f_poly, st);
+      e = (bn_sq == 256) ? launch_gemm<256, false, kEpiPoly, true>(S.k128, S.kbn, S.kbn, q, f_poly, st)
+                         : launch_gemm<128, false, kEpiPoly, true>(S.k128, S.kbn, S.kbn, q, f_poly, st);
       if (e != cudaSuccess) return e;
     }
 
@@ -465,12 +579,17 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.total_tiles = u.tiles_per_matrix * batch;
     u.out = xb[cur ^ 1]; u.out_ld = m; u.out_bstride = static_cast<int64_t>(n) * m;
     u.aux = xb[cur]; u.aux_ld = m; u.aux_bstride = static_cast<int64_t>(n) * m;
-    u.ca = ca; u.cb = (cc != 0.f) ? 1.f : cb; u.cc = 0.f;
+    u.lo_off = a.lo_off;
+    u.ca = 1.f; u.cb = 1.f; u.cc = 0.f; u.cd = 0.f;
+    u.pdiag_in = a.pdiag; u.pdiag_bstride = n;
+    u.kplanes = (it < kResidualIters) ? 2 : 1;
+    u.lo_in = it < kLoIters;
+    u.lo_out = it + 1 < kLoIters;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
-    const CUtensorMap& lhs = (cc != 0.f) ? P.k128 : S.k128;
-    e = (bn_up == 256) ? launch_gemm<256, true, kEpiUpdate, false>(lhs, X[cur].mn, u, f_update, st)
-                       : launch_gemm<128, true, kEpiUpdate, false>(lhs, X[cur].mn, u, f_update, st);
+    e = (bn_up == 256)
+            ? launch_gemm<256, true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st)
+            : launch_gemm<128, true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

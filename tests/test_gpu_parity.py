@@ -76,6 +76,10 @@ ISOLATING_SCHEDULES = {
 @pytest.mark.parametrize("name", sorted(ISOLATING_SCHEDULES))
 @pytest.mark.parametrize("rows,cols", [(256, 512), (384, 256), (512, 512)])
 def test_ns_single_stage_schedules(name, rows, cols):
+    """One-iteration schedules that isolate the kernels, at the O' bar.  The
+    library evaluates X + (bS + cS^2 + (a-1)I) X, so schedules with a = 0
+    (gram, square) cancel X against -X and keep fewer digits than the
+    hybrid schedule does."""
     stages = ISOLATING_SCHEDULES[name]
     sched = m.Schedule(stages)
     rng = np.random.default_rng(7)
@@ -83,7 +87,7 @@ def test_ns_single_stage_schedules(name, rows, cols):
     got = run_ns(x, sched)
     want = oracle_ns_batch(x, stages)
     for b in range(2):
-        assert rel_fro(f64(got[b]), want[b]) <= 1.5e-2
+        assert rel_fro(f64(got[b]), want[b]) <= NS_TOL
 
 
 def test_ns_without_normalisation_fixes_orthonormal_rows():

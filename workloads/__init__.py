@@ -167,16 +167,20 @@ def dense_layers(seed: int = 3, layers: int = 32, device="cuda", spike_rank: int
     return out
 
 
-def moe_experts(seed: int = 4, experts: int = 256, device="cuda", nu: float = 3.0) -> dict:
-    """{name: (W bf16 [E, r, c], G bf16, M fp32)}; G = 1e-3 * Student-t(nu)."""
+def moe_experts(seed: int = 4, experts: int = 256, device="cuda", nu: int = 3,
+                only: tuple = ()) -> dict:
+    """{name: (W bf16 [E, r, c], G bf16, M fp32)}; G = 1e-3 * Student-t(nu), drawn as
+    z / sqrt(chi2_nu / nu) with chi2_nu a sum of nu squared standard normals."""
     gen = _device_gen(device, seed)
     out = {}
     for name, r, c in MOE_SHAPES:
+        if only and name not in only:
+            continue
         W = (torch.randn(experts, r, c, generator=gen, device=device) * W_STD).to(torch.bfloat16)
+        chi2 = torch.zeros(experts, r, c, device=device)
+        for _ in range(int(nu)):
+            chi2.add_(torch.randn(experts, r, c, generator=gen, device=device).square_())
         z = torch.randn(experts, r, c, generator=gen, device=device)
-        # Student-t(nu) = z / sqrt(chi2_nu / nu), chi2_nu = 2 * Gamma(nu/2, 1)
-        chi2 = 2.0 * torch._standard_gamma(torch.full((experts, r, c), nu / 2, device=device),
-                                           generator=gen)
         G = (G_STD * z / torch.sqrt(chi2 / nu)).to(torch.bfloat16)
         out[name] = (W, G, torch.zeros(experts, r, c, device=device))
         del z, chi2
