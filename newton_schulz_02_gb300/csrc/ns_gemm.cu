@@ -62,6 +62,7 @@ namespace {
 constexpr int kBM = 128;  // tile rows (TMEM lanes)
 constexpr int kResidualIters = 2;  // iterations whose product also reads the lo plane
 constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
+constexpr bool kUsePairs = true;   // 2-CTA clusters sharing the B tile (see k_ns_gemm)
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
@@ -122,6 +123,39 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& b, 
   }
 }
 
+// Work unit t -> (matrix, tile row, tile column).  With PAIR the unit is a
+// pair of vertically adjacent tiles (tm = 2 pm + cluster rank) sharing the
+// tile column; for symmetric outputs (BN = 256) a pair is one upper
+// super-block row segment (pm = super-row).
+template <int BN, bool SYM, bool PAIR>
+__device__ __forceinline__ void decode_unit(const GemmParams& p, int t, uint32_t rank, int& b,
+                                            int& tm, int& tn) {
+  if (!PAIR) {
+    decode_tile<BN, SYM>(p, t, b, tm, tn);
+    return;
+  }
+  b = t / p.tiles_per_matrix;
+  int l = t - b * p.tiles_per_matrix;
+  int pm = 0;
+  tn = 0;
+  if (!SYM) {
+    pm = l / p.tiles_n;
+    tn = l - pm * p.tiles_n;
+  } else {
+    const int S = p.tiles_n;
+    for (int sr = 0; sr < S; ++sr) {
+      const int cnt = S - sr;
+      if (l < cnt) {
+        pm = sr;
+        tn = sr + l;
+        break;
+      }
+      l -= cnt;
+    }
+  }
+  tm = 2 * pm + static_cast<int>(rank);
+}
+
 // A drain wait: ignores the abort flag, still bounded.
 __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, uint32_t* status,
                                                 uint64_t timeout_ns) {
@@ -154,10 +188,17 @@ __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32])
   }
 }
 
-template <int BN, bool B_MN, int EPI, bool SYM>
+// PAIR: launched in clusters of two CTAs that compute vertically adjacent
+// tiles of the same tile column.  Each CTA loads its own A tile and half of
+// the shared B tile, multicasting that half into both CTAs' shared memory,
+// so each CTA fetches 32 KB instead of 48 KB per k-block from L2.  A stage is
+// refilled only after both CTAs' MMAs have consumed it (each MMA commit
+// arrives on the stage's empty barrier in both CTAs).
+template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+  static_assert(!(SYM && PAIR) || BN == 256, "symmetric pairs are 256-row super-rows");
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, B_MN);
@@ -176,11 +217,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], PAIR ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -200,6 +244,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int nkb = p.K / kBK;
@@ -211,9 +256,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         int b, tm, tn;
-        decode_tile<BN, SYM>(p, t, b, tm, tn);
+        decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
         for (int kb = 0; kb < nkb_total; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
@@ -224,7 +269,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const CUtensorMap* tb = second ? &tmB2 : &tmB;
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_3d(smA + stage * C::kABytes, &tmA, &full[stage], k0, tm * kBM, b);
-          if (!B_MN) {
+          if (PAIR) {
+            // this CTA's half of B, into both CTAs (the B map's box is half the tile)
+            if (!B_MN) {
+              tma_load_3d_multicast(smB + stage * C::kBBytes + rank * (C::kBBytes / 2), tb,
+                                    &full[stage], k0, tn * BN + static_cast<int>(rank) * (BN / 2),
+                                    b, 0x3);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j) {
+                const int jj = static_cast<int>(rank) * (BN / 128) + j;
+                tma_load_3d_multicast(smB + stage * C::kBBytes + jj * (64 * kBK * 2), tb,
+                                      &full[stage], tn * BN + jj * 64, k0, b, 0x3);
+              }
+            }
+          } else if (!B_MN) {
             tma_load_3d(smB + stage * C::kBBytes, tb, &full[stage], k0, tn * BN, b);
           } else {
 #pragma unroll
@@ -250,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns))
           break;
         tc_fence_after();
@@ -279,7 +338,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);
+          if (PAIR)
+            tc_commit_multicast(&empty[stage], 0x3);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -307,9 +369,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int c_begin = (ep >> 2) * kChunksPerWarp;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
-      decode_tile<BN, SYM>(p, t, b, tm, tn);
+      decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
       const int row0 = tm * kBM + q * 32;
       const int row = row0 + lane;
       const bool mirror = SYM && (tn > tm / (BN / kBM));
@@ -423,6 +485,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // no CTA leaves while its peer may still write into it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -483,19 +546,41 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int batch, int K, int N) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_MN, int EPI, bool SYM>
+template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
                         const GemmParams& p, double alg_flops, cudaStream_t st) {
-  auto kern = k_ns_gemm<BN, B_MN, EPI, SYM>;
+  auto kern = k_ns_gemm<BN, B_MN, EPI, SYM, PAIR>;
   const size_t smem = Cfg<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = std::max(1, std::min(p.total_tiles, sm_count()));
   const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  int units_in_flight = sm_count();
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    units_in_flight = clusters;
+  }
+  const int units = std::max(1, std::min(p.total_tiles, units_in_flight));
+  cfg.gridDim = dim3(PAIR ? 2 * units : units);
   prof_begin(kind, st);
-  kern<<<grid, kGemmThreads, smem, st>>>(ta, tb, tb2, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -542,10 +627,14 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     const bool first = (it == 0);
     cudaError_t e;
 
+    // Pair clusters whenever the tile rows come in pairs (n_pad % 256 == 0).
+    const bool pair = kUsePairs && (n % 256 == 0);
+
     GemmParams g{};
     g.M = n; g.N = n; g.K = m;
-    g.tiles_m = tm_sq; g.tiles_n = S_sq; g.tiles_per_matrix = sym_tiles;
-    g.total_tiles = sym_tiles * batch;
+    g.tiles_m = tm_sq; g.tiles_n = S_sq;
+    g.tiles_per_matrix = (pair && bn_sq == 256) ? S_sq * (S_sq + 1) / 2 : sym_tiles;
+    g.total_tiles = g.tiles_per_matrix * batch;
     g.out = (cc != 0.f) ? a.A : a.B;   // c == 0: the Gram epilogue writes P directly
     g.out_ld = n; g.out_bstride = static_cast<int64_t>(n) * n;
     g.cb = (cc != 0.f) ? 1.f : cb;
@@ -555,9 +644,12 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.kplanes = 1;
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    e = (bn_sq == 256)
-            ? launch_gemm<256, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st)
-            : launch_gemm<128, false, kEpiGram, true>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
+    if (bn_sq == 256 && pair)
+      e = launch_gemm<256, false, kEpiGram, true, true>(X[cur].k128, X[cur].k128, X[cur].k128, g, f_gram, st);
+    else if (bn_sq == 256)
+      e = launch_gemm<256, false, kEpiGram, true, false>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
+    else
+      e = launch_gemm<128, false, kEpiGram, true, false>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
     if (e != cudaSuccess) return e;
 
     if (cc != 0.f) {
@@ -568,14 +660,19 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.cb = cb; q.cc = cc; q.cd = ca - 1.f;
       q.pdiag = a.pdiag;
       q.mscale = nullptr;
-      e = (bn_sq == 256) ? launch_gemm<256, false, kEpiPoly, true>(S.k128, S.kbn, S.kbn, q, f_poly, st)
-                         : launch_gemm<128, false, kEpiPoly, true>(S.k128, S.kbn, S.kbn, q, f_poly, st);
+      if (bn_sq == 256 && pair)
+        e = launch_gemm<256, false, kEpiPoly, true, true>(S.k128, S.k128, S.k128, q, f_poly, st);
+      else if (bn_sq == 256)
+        e = launch_gemm<256, false, kEpiPoly, true, false>(S.k128, S.kbn, S.kbn, q, f_poly, st);
+      else
+        e = launch_gemm<128, false, kEpiPoly, true, false>(S.k128, S.kbn, S.kbn, q, f_poly, st);
       if (e != cudaSuccess) return e;
     }
 
     GemmParams u{};
     u.M = n; u.N = m; u.K = n;
-    u.tiles_m = n / kBM; u.tiles_n = m / bn_up; u.tiles_per_matrix = u.tiles_m * u.tiles_n;
+    u.tiles_m = n / kBM; u.tiles_n = m / bn_up;
+    u.tiles_per_matrix = pair ? (u.tiles_m / 2) * u.tiles_n : u.tiles_m * u.tiles_n;
     u.total_tiles = u.tiles_per_matrix * batch;
     u.out = xb[cur ^ 1]; u.out_ld = m; u.out_bstride = static_cast<int64_t>(n) * m;
     u.aux = xb[cur]; u.aux_ld = m; u.aux_bstride = static_cast<int64_t>(n) * m;
@@ -587,9 +684,14 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.lo_out = it + 1 < kLoIters;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
-    e = (bn_up == 256)
-            ? launch_gemm<256, true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st)
-            : launch_gemm<128, true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+    if (bn_up == 256 && pair)
+      e = launch_gemm<256, true, kEpiUpdate, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+    else if (bn_up == 256)
+      e = launch_gemm<256, true, kEpiUpdate, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+    else if (pair)
+      e = launch_gemm<128, true, kEpiUpdate, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+    else
+      e = launch_gemm<128, true, kEpiUpdate, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
