@@ -16,7 +16,11 @@
 // Frobenius normalisation is folded into the first iteration: with
 // s = ||X||_F, S_0 = (X X^T)/s^2 and X_1 = (X + P_0 X)/s.
 //
-// Kernel shape (one persistent CTA per SM, 6 warps):
+// Kernel shapes (one persistent CTA per SM, 6 warps).  Where tile rows come
+// in pairs and BN = 256, k_ns_gemm2 runs each 256 x 256 tile on a CTA pair
+// with pair-wide tcgen05 MMAs (cta_group::2); otherwise k_ns_gemm runs
+// 128 x BN tiles per CTA (in multicast pairs when tile rows pair up).
+// Roles:
 //   warp 0      one thread issues TMA loads of A and B k-blocks into a
 //               multi-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates TMEM and one thread issues tcgen05.mma
@@ -63,6 +67,10 @@ constexpr int kBM = 128;  // tile rows (TMEM lanes)
 constexpr int kResidualIters = 2;  // iterations whose product also reads the lo plane
 constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
 constexpr bool kUsePairs = true;   // 2-CTA clusters sharing the B tile (see k_ns_gemm)
+#ifndef MUON_TWO_SM
+#define MUON_TWO_SM 1
+#endif
+constexpr bool kUseTwoSm = MUON_TWO_SM != 0;  // pair-wide MMA (k_ns_gemm2) where BN = 256
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
@@ -186,6 +194,124 @@ __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32])
       v[q * 8 + 2 * k + 1] = f.y;
     }
   }
+}
+
+// Epilogue of one 128 x BN tile for the calling warp (TMEM lane quarter q,
+// rows tm*128 + q*32 + lane): waits for the accumulator (tfull_bar, parity),
+// applies the kernel's epilogue and stores.  The residual operand of the next
+// 32-column chunk is loaded while the current chunk is finished.  (Staging the
+// mirrored store through shared memory was slower: it competes with the
+// tensor core for shared-memory bandwidth.)  Returns false if the wait gave up.
+template <int BN, int EPI, bool SYM>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_acc, int b, int tm,
+                                              int tn, int q, int lane, uint64_t* tfull_bar,
+                                              uint32_t parity, volatile int* abort_flag) {
+  constexpr int kChunksPerWarp = BN / 32;
+  constexpr int c_begin = 0;
+  const int row0 = tm * kBM + q * 32;
+  const int row = row0 + lane;
+  const bool mirror = SYM && (tn > tm / (BN / kBM));
+  const __nv_bfloat16* aux_row =
+      (EPI == kEpiGram) ? nullptr
+                        : p.aux + static_cast<int64_t>(b) * p.aux_bstride +
+                              static_cast<int64_t>(row) * p.aux_ld + tn * BN;
+  uint4 cur_h[4], cur_l[4], nxt_h[4], nxt_l[4];
+  const bool lo_in = (EPI == kEpiUpdate) && p.lo_in;
+  const bool lo_out = (EPI == kEpiUpdate) && p.lo_out;
+  if (EPI != kEpiGram) {
+    load_raw4(aux_row + c_begin * 32, cur_h);
+    if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
+  }
+  if (!mbar_wait_bounded(tfull_bar, parity, abort_flag, p.status, p.timeout_ns)) return false;
+  tc_fence_after();
+  float ms = 1.f;
+  if (p.mscale != nullptr) ms = p.mscale[b];
+  __nv_bfloat16* out = p.out + static_cast<int64_t>(b) * p.out_bstride;
+  const uint32_t t_row = t_acc + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+  for (int i = 0; i < kChunksPerWarp; ++i) {
+    const int c = c_begin + i;
+    if (EPI != kEpiGram && i + 1 < kChunksPerWarp) {
+      load_raw4(aux_row + (c + 1) * 32, nxt_h);
+      if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
+    }
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, r);
+    tmem_ld_wait(r);
+    const int col0 = tn * BN + c * 32;
+    float v[32];
+    if (EPI == kEpiGram) {
+      const float s2 = ms * ms * p.cb;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s2;
+    } else {
+      float x[32];
+      unpack_raw4(cur_h, x);
+      if (EPI == kEpiPoly) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cc, __uint_as_float(r[e]), p.cb * x[e]);
+      } else {
+        float xl[32];
+        if (lo_in) {
+          unpack_raw4(cur_l, xl);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xl[e] = 0.f;
+        }
+        const float d = p.pdiag_in[static_cast<int64_t>(b) * p.pdiag_bstride + row];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float xe = x[e] + xl[e];
+          v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
+        }
+      }
+    }
+    if (EPI != kEpiUpdate && p.pdiag != nullptr && row >= col0 && row < col0 + 32) {
+      // the (a - 1) I shift; the diagonal's bf16 rounding residual is kept
+      // in fp32 so that P's diagonal is exact to fp32 in the update
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (col0 + e == row) {
+          v[e] += p.cd;
+          p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
+              v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+        }
+    }
+    __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
+    uint4* dst = reinterpret_cast<uint4*>(drow);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 u, ul;
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+      __nv_bfloat162* hl = reinterpret_cast<__nv_bfloat162*>(&ul);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v0 = v[8 * k + 2 * e], v1 = v[8 * k + 2 * e + 1];
+        h[e] = __floats2bfloat162_rn(v0, v1);
+        if (lo_out) {
+          const float2 f = __bfloat1622float2(h[e]);
+          hl[e] = __floats2bfloat162_rn(v0 - f.x, v1 - f.y);
+        }
+      }
+      dst[k] = u;
+      if (lo_out) reinterpret_cast<uint4*>(drow + p.lo_off)[k] = ul;
+    }
+    if (mirror) {
+      // transposed copy: for each column e the warp's 32 lanes (32
+      // consecutive rows) store 64 contiguous bytes of row col0 + e
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = __float2bfloat16_rn(v[e]);
+    }
+    if (EPI != kEpiGram) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        cur_h[k] = nxt_h[k];
+        if (lo_in) cur_l[k] = nxt_l[k];
+      }
+    }
+  }
+  return true;
 }
 
 // PAIR: launched in clusters of two CTAs that compute vertically adjacent
@@ -358,124 +484,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
-    // Warps 2..5, one per TMEM lane quarter (warp & 3).  The residual operand
-    // of the next 32-column chunk is loaded while the current chunk is
-    // finished.  (Staging the mirrored store through shared memory was
-    // slower: it competes with the tensor core for shared-memory bandwidth.)
-    constexpr int kChunks = BN / 32;
-    constexpr int kChunksPerWarp = kChunks / (kEpiWarps / 4);
-    const int q = warp & 3;
-    const int ep = warp - 2;
-    const int c_begin = (ep >> 2) * kChunksPerWarp;
+    const int q = warp & 3;  // TMEM lane quarter of this warp
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
       decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
-      const int row0 = tm * kBM + q * 32;
-      const int row = row0 + lane;
-      const bool mirror = SYM && (tn > tm / (BN / kBM));
-      const __nv_bfloat16* aux_row =
-          (EPI == kEpiGram) ? nullptr
-                            : p.aux + static_cast<int64_t>(b) * p.aux_bstride +
-                                  static_cast<int64_t>(row) * p.aux_ld + tn * BN;
-      uint4 cur_h[4], cur_l[4], nxt_h[4], nxt_l[4];
-      const bool lo_in = (EPI == kEpiUpdate) && p.lo_in;
-      const bool lo_out = (EPI == kEpiUpdate) && p.lo_out;
-      if (EPI != kEpiGram) {
-        load_raw4(aux_row + c_begin * 32, cur_h);
-        if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
-      }
-      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort_flag, p.status, p.timeout_ns)) break;
-      tc_fence_after();
-      float ms = 1.f;
-      if (p.mscale != nullptr) ms = p.mscale[b];
-      __nv_bfloat16* out = p.out + static_cast<int64_t>(b) * p.out_bstride;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int i = 0; i < kChunksPerWarp; ++i) {
-        const int c = c_begin + i;
-        if (EPI != kEpiGram && i + 1 < kChunksPerWarp) {
-          load_raw4(aux_row + (c + 1) * 32, nxt_h);
-          if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
-        }
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tmem_ld_wait(r);
-        const int col0 = tn * BN + c * 32;
-        float v[32];
-        if (EPI == kEpiGram) {
-          const float s2 = ms * ms * p.cb;
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s2;
-        } else {
-          float x[32];
-          unpack_raw4(cur_h, x);
-          if (EPI == kEpiPoly) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cc, __uint_as_float(r[e]), p.cb * x[e]);
-          } else {
-            float xl[32];
-            if (lo_in) {
-              unpack_raw4(cur_l, xl);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) xl[e] = 0.f;
-            }
-            const float d = p.pdiag_in[static_cast<int64_t>(b) * p.pdiag_bstride + row];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float xe = x[e] + xl[e];
-              v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
-            }
-          }
-        }
-        if (EPI != kEpiUpdate && p.pdiag != nullptr && row >= col0 && row < col0 + 32) {
-          // the (a - 1) I shift; the diagonal's bf16 rounding residual is kept
-          // in fp32 so that P's diagonal is exact to fp32 in the update
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (col0 + e == row) {
-              v[e] += p.cd;
-              p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
-                  v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
-            }
-        }
-        __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
-        uint4* dst = reinterpret_cast<uint4*>(drow);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 u, ul;
-          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-          __nv_bfloat162* hl = reinterpret_cast<__nv_bfloat162*>(&ul);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v0 = v[8 * k + 2 * e], v1 = v[8 * k + 2 * e + 1];
-            h[e] = __floats2bfloat162_rn(v0, v1);
-            if (lo_out) {
-              const float2 f = __bfloat1622float2(h[e]);
-              hl[e] = __floats2bfloat162_rn(v0 - f.x, v1 - f.y);
-            }
-          }
-          dst[k] = u;
-          if (lo_out) reinterpret_cast<uint4*>(drow + p.lo_off)[k] = ul;
-        }
-        if (mirror) {
-          // transposed copy: for each column e the warp's 32 lanes (32
-          // consecutive rows) store 64 contiguous bytes of row col0 + e
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = __float2bfloat16_rn(v[e]);
-        }
-        if (EPI != kEpiGram) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            cur_h[k] = nxt_h[k];
-            if (lo_in) cur_l[k] = nxt_l[k];
-          }
-        }
-      }
+      if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
+                                       q, lane, &tfull[acc], acc_phase, abort_flag))
+        break;
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -490,6 +507,199 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+
+// Pair-wide (2-SM) variant, BN = 256: the CTA pair computes a 256 x 256 tile
+// with one tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16) per k-step,
+// issued by the even CTA.  Each CTA stages only its own 128 rows of A and its
+// half (128 rows, or 128 columns when MN-major) of B, so a stage is 32 KB per
+// CTA and six stages fit; both CTAs' loads complete on the even CTA's full
+// barrier.  D is split across the two CTAs' tensor memory (128 rows each);
+// each CTA's epilogue drains its own rows and reports to the even CTA's
+// accumulator-empty barrier.
+#ifndef MUON_TWO_SM_ACC
+#define MUON_TWO_SM_ACC 2
+#endif
+constexpr int kAccBufs2 = MUON_TWO_SM_ACC;  // TMEM accumulators per CTA (256 columns each)
+constexpr int kStages2 = 6;
+constexpr uint32_t kHalfBytes2 = 128 * kBK * 2;      // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kStageBytes2 = 2 * kHalfBytes2;   // A + B half, per CTA
+constexpr size_t kSmemBytes2 = kStages2 * kStageBytes2 + 1024 + 256;
+
+template <bool B_MN, int EPI, bool SYM>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_ns_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+  constexpr int BN = 256;
+  constexpr uint32_t kTmemCols = kAccBufs2 * BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, B_MN);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages2 * kHalfBytes2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStageBytes2);
+  uint64_t* empty = full + kStages2;
+  uint64_t* tfull = empty + kStages2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int unit0 = static_cast<int>(blockIdx.x >> 1);
+  const int ustep = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(&full[s], 1);    // the even CTA's arrive_expect_tx; bytes from both CTAs
+      mbar_init(&empty[s], 1);   // the even CTA's MMA commit, multicast to both
+    }
+    for (int a = 0; a < kAccBufs2; ++a) {
+      mbar_init(&tfull[a], 1);                 // MMA commit, multicast to both
+      mbar_init(&tempty[a], 2 * kEpiWarps);    // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (p.kplanes > 1) tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int nkb = p.K / kBK;
+  const int nkb_total = nkb * p.kplanes;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint32_t full0 = mapa_shared(&full[0], 0);  // the even CTA's full barriers
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
+        int b, tm, tn;
+        decode_unit<BN, SYM, true>(p, t, rank, b, tm, tn);
+        for (int kb = 0; kb < nkb_total; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const bool second = kb >= nkb;
+          const int k0 = (second ? kb - nkb : kb) * kBK;
+          const CUtensorMap* tb = second ? &tmB2 : &tmB;
+          const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes2);
+          tma_load_3d_pair(smA + stage * kHalfBytes2, &tmA, bar, k0, tm * kBM, b);
+          if (!B_MN) {
+            tma_load_3d_pair(smB + stage * kHalfBytes2, tb, bar, k0,
+                             tn * BN + static_cast<int>(rank) * 128, b);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_load_3d_pair(smB + stage * kHalfBytes2 + j * (64 * kBK * 2), tb, bar,
+                               tn * BN + (static_cast<int>(rank) * 2 + j) * 64, k0, b);
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // The even CTA's full barriers count both CTAs' bytes: draining them
+      // there covers every load of the pair.
+      if (leader)
+        for (int s = 0; s < kStages2; ++s)
+          if ((issued >> s) & 1u)
+            mbar_wait_drain(&full[s], (last_par >> s) & 1u, p.status, p.timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nkb_total; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smA + stage * kHalfBytes2);
+          const uint32_t b_addr = smem_u32(smB + stage * kHalfBytes2);
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + ks * 16 * 128, kBK * 128, 1024)
+                                     : smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&tfull[acc], 0x3);
+        if (++acc == kAccBufs2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      tc_commit_pair_multicast(drain, 0x1);
+      mbar_wait_drain(drain, 0, p.status, p.timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = unit0; t < p.total_tiles; t += ustep) {
+      int b, tm, tn;
+      decode_unit<BN, SYM, true>(p, t, rank, b, tm, tn);
+      if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
+                                       q, lane, &tfull[acc], acc_phase, abort_flag))
+        break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      if (++acc == kAccBufs2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -584,6 +794,40 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   return cudaGetLastError();
 }
 
+
+template <bool B_MN, int EPI, bool SYM>
+cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
+                         const GemmParams& p, double alg_flops, cudaStream_t st) {
+  auto kern = k_ns_gemm2<B_MN, EPI, SYM>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes2));
+  if (e != cudaSuccess) return e;
+  const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kSmemBytes2;
+  cfg.stream = st;
+  cfg.gridDim = dim3(2);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const int units = std::max(1, std::min(p.total_tiles, clusters));
+  cfg.gridDim = dim3(2 * units);
+  prof_begin(kind, st);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
+  prof_end(kind, st, alg_flops, 0.0);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 struct OperandMaps {
   CUtensorMap k128, kbn, mn, mn_lo;
 };
@@ -644,7 +888,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.kplanes = 1;
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    if (bn_sq == 256 && pair)
+    if (bn_sq == 256 && pair && kUseTwoSm)
+      e = launch_gemm2<false, kEpiGram, true>(X[cur].k128, X[cur].k128, X[cur].k128, g, f_gram, st);
+    else if (bn_sq == 256 && pair)
       e = launch_gemm<256, false, kEpiGram, true, true>(X[cur].k128, X[cur].k128, X[cur].k128, g, f_gram, st);
     else if (bn_sq == 256)
       e = launch_gemm<256, false, kEpiGram, true, false>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
@@ -660,7 +906,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.cb = cb; q.cc = cc; q.cd = ca - 1.f;
       q.pdiag = a.pdiag;
       q.mscale = nullptr;
-      if (bn_sq == 256 && pair)
+      if (bn_sq == 256 && pair && kUseTwoSm)
+        e = launch_gemm2<false, kEpiPoly, true>(S.k128, S.k128, S.k128, q, f_poly, st);
+      else if (bn_sq == 256 && pair)
         e = launch_gemm<256, false, kEpiPoly, true, true>(S.k128, S.k128, S.k128, q, f_poly, st);
       else if (bn_sq == 256)
         e = launch_gemm<256, false, kEpiPoly, true, false>(S.k128, S.kbn, S.kbn, q, f_poly, st);
@@ -684,7 +932,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.lo_out = it + 1 < kLoIters;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
-    if (bn_up == 256 && pair)
+    if (bn_up == 256 && pair && kUseTwoSm)
+      e = launch_gemm2<true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+    else if (bn_up == 256 && pair)
       e = launch_gemm<256, true, kEpiUpdate, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
     else if (bn_up == 256)
       e = launch_gemm<256, true, kEpiUpdate, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
