@@ -287,6 +287,7 @@ __device__ __forceinline__ void* apply_base(const ApplyArgs& p, int b) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_apply_wide(ApplyArgs p) {
+  griddep_wait();  // launched as a programmatic dependent of the last GEMM
   const int b = blockIdx.y;
   if (p.skip[b]) return;
   void* wbase = apply_base(p, b);
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(kThreads) k_apply_wide(ApplyArgs p) {
 // ---- last pass, tall: W[i][j] from X_ws[j][i] ----------------------------------------
 __global__ void __launch_bounds__(kThreads) k_apply_tall(ApplyArgs p) {
   __shared__ float tile[kTile][kTile + 1];
+  griddep_wait();  // launched as a programmatic dependent of the last GEMM
   const int b = blockIdx.y;
   if (p.skip[b]) return;
   void* wbase = apply_base(p, b);
@@ -414,12 +416,22 @@ cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st) {
   const double elems = static_cast<double>(a.batch) * a.rows * a.cols;
   const double wsz = a.w_dtype == MUON_BF16 ? 2.0 : 4.0;
   const double per = (a.has_lo ? 4.0 : 2.0) + (a.mode == 0 ? 2.0 * wsz : wsz);
+  // programmatic dependent of the previous kernel (the last Newton–Schulz
+  // GEMM, a persistent grid whose CTAs are all resident)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_begin(kKindApply, st);
-  if (a.tall)
-    k_apply_tall<<<grid, kThreads, 0, st>>>(a);
-  else
-    k_apply_wide<<<grid, kThreads, 0, st>>>(a);
+  const cudaError_t e = a.tall ? cudaLaunchKernelEx(&cfg, k_apply_tall, a)
+                               : cudaLaunchKernelEx(&cfg, k_apply_wide, a);
   prof_end(kKindApply, st, 0.0, elems * per);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -67,6 +67,13 @@ constexpr int kBM = 128;  // tile rows (TMEM lanes)
 constexpr int kResidualIters = 2;  // iterations whose product also reads the lo plane
 constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
 constexpr bool kUsePairs = true;   // 2-CTA clusters sharing the B tile (see k_ns_gemm)
+#ifndef MUON_PDL
+#define MUON_PDL 1
+#endif
+// Launch the GEMMs as programmatic dependents of the previous kernel: their
+// set-up (barriers, TMEM allocation, descriptor prefetch) overlaps its tail,
+// and griddepcontrol.wait holds every dependent read until it has finished.
+constexpr bool kUsePdl = MUON_PDL != 0;
 #ifndef MUON_TWO_SM
 #define MUON_TWO_SM 1
 #endif
@@ -202,12 +209,11 @@ __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32])
 // 32-column chunk is loaded while the current chunk is finished.  (Staging the
 // mirrored store through shared memory was slower: it competes with the
 // tensor core for shared-memory bandwidth.)  Returns false if the wait gave up.
-template <int BN, int EPI, bool SYM>
+template <int BN, int EPI, bool SYM, int kChunksPerWarp = BN / 32>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_acc, int b, int tm,
                                               int tn, int q, int lane, uint64_t* tfull_bar,
-                                              uint32_t parity, volatile int* abort_flag) {
-  constexpr int kChunksPerWarp = BN / 32;
-  constexpr int c_begin = 0;
+                                              uint32_t parity, volatile int* abort_flag,
+                                              int c_begin = 0) {
   const int row0 = tm * kBM + q * 32;
   const int row = row0 + lane;
   const bool mirror = SYM && (tn > tm / (BN / kBM));
@@ -373,6 +379,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();  // the previous kernel's outputs are this kernel's inputs
   const int nkb = p.K / kBK;
   const int nkb_total = nkb * p.kplanes;
 
@@ -524,12 +532,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #endif
 constexpr int kAccBufs2 = MUON_TWO_SM_ACC;  // TMEM accumulators per CTA (256 columns each)
 constexpr int kStages2 = 6;
+#ifndef MUON_EPI2_WARPS
+#define MUON_EPI2_WARPS 8
+#endif
+constexpr int kEpiWarps2 = MUON_EPI2_WARPS;             // 4 or 8 (two per TMEM lane quarter)
+constexpr int kGemmThreads2 = 64 + 32 * kEpiWarps2;
 constexpr uint32_t kHalfBytes2 = 128 * kBK * 2;      // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kStageBytes2 = 2 * kHalfBytes2;   // A + B half, per CTA
 constexpr size_t kSmemBytes2 = kStages2 * kStageBytes2 + 1024 + 256;
 
 template <bool B_MN, int EPI, bool SYM>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads2, 1)
     k_ns_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int BN = 256;
@@ -562,7 +575,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < kAccBufs2; ++a) {
       mbar_init(&tfull[a], 1);                 // MMA commit, multicast to both
-      mbar_init(&tempty[a], 2 * kEpiWarps);    // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], 2 * kEpiWarps2);   // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -581,6 +594,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();  // the previous kernel's outputs are this kernel's inputs
   const int nkb = p.K / kBK;
   const int nkb_total = nkb * p.kplanes;
 
@@ -674,14 +689,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;
+    constexpr int kChunksPerWarp2 = (BN / 32) / (kEpiWarps2 / 4);
+    const int c_begin = ((warp - 2) >> 2) * kChunksPerWarp2;
     const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
       decode_unit<BN, SYM, true>(p, t, rank, b, tm, tn);
-      if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
-                                       q, lane, &tfull[acc], acc_phase, abort_flag))
+      if (!epilogue_tile<BN, EPI, SYM, kChunksPerWarp2>(
+              p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
+              acc_phase, abort_flag, c_begin))
         break;
       tc_fence_before();
       __syncwarp();
@@ -766,17 +784,17 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   if (e != cudaSuccess) return e;
   const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
+  cfg.attrs = attr;
   int units_in_flight = sm_count();
   if (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2);
     int clusters = 0;
@@ -787,6 +805,11 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
   }
   const int units = std::max(1, std::min(p.total_tiles, units_in_flight));
   cfg.gridDim = dim3(PAIR ? 2 * units : units);
+  if (kUsePdl) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs += 1;
+  }
   prof_begin(kind, st);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);
@@ -804,14 +827,14 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
   if (e != cudaSuccess) return e;
   const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(kGemmThreads2);
   cfg.dynamicSmemBytes = kSmemBytes2;
   cfg.stream = st;
   cfg.gridDim = dim3(2);
@@ -821,6 +844,11 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
   if (clusters < 1) return cudaErrorInvalidConfiguration;
   const int units = std::max(1, std::min(p.total_tiles, clusters));
   cfg.gridDim = dim3(2 * units);
+  if (kUsePdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   prof_begin(kind, st);
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);

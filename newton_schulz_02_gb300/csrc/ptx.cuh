@@ -123,6 +123,20 @@ __device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const void
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Let the next kernel in the stream start launching (its CTAs take SMs as
+// this grid's CTAs leave them).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel in the stream has completed and its writes
+// are visible (returns at once when this grid was not launched as a
+// programmatic dependent).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // thread-block clusters
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
