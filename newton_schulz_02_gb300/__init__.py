@@ -231,6 +231,21 @@ class Group:
                    wd_mask, fan_out_axis=1)
 
 
+def split_rows(W: torch.Tensor, G: torch.Tensor, M: torch.Tensor, parts: int,
+               wd_mask=None) -> Group:
+    """A fused weight stacked along rows (e.g. an FC1 [gate; up] weight,
+    [parts*rows, cols]) as `parts` sub-matrices rows x cols orthogonalised
+    separately (split_linear_fc1; each part keeps fan_out = its rows)."""
+    if W.shape[0] % parts != 0:
+        raise ValueError("rows must split into equal parts")
+    r = W.shape[0] // parts
+    sl = [slice(k * r, (k + 1) * r) for k in range(parts)]
+    return Group([W[s] for s in sl], [G[s] for s in sl], [M[s] for s in sl], wd_mask, fan_out_axis=0)
+
+
+Group.split_rows = staticmethod(split_rows)
+
+
 def _group_array(groups: Sequence[Group]):
     arr = (muon_group_t * len(groups))(*[g.c for g in groups])
     return arr

@@ -86,6 +86,24 @@ struct ApplyArgs {
   const float* oscale;       // per-matrix factor on O' (zero-iteration schedules), or nullptr
 };
 
+// Last-iteration store fused into the update epilogue: mode 1 applies
+// W <- W*(1 - lr*wd*mask) - lr*scale*O' (muon_step_batched), mode 2 writes O'
+// into a dense output (newton_schulz_batched); mode 0 keeps the iterate in the
+// workspace for a separate last pass.
+struct FinalStore {
+  int mode;
+  int rows, cols;            // W / output shape in its own orientation
+  int tall;                  // rows > cols: the wide element (i, j) is W[j][i]
+  int dtype;                 // W dtype (mode 1) or output dtype (mode 2)
+  void* const* w_ptrs;       // mode 1: device array of W pointers
+  int64_t w_ld;              // mode 1: W row stride (elements)
+  void* out_base;            // mode 2: dense [batch][rows][cols]
+  const uint8_t* wd_mask;    // mode 1: decay mask, or nullptr (all on)
+  const uint8_t* skip;       // matrices to leave untouched
+  float decay_on;            // 1 - lr*wd
+  float lr_scale;            // lr * scale
+};
+
 struct NsChainArgs {
   int batch, n_pad, m_pad;
   int n, m;             // unpadded sizes (algorithmic flop counts)
@@ -98,6 +116,7 @@ struct NsChainArgs {
   const float* inv_s;   // folded into the first iteration; nullptr = no normalisation
   const float* coeffs;  // host [iters][3]
   int iters;
+  FinalStore fin;       // fused into the last iteration when fin.mode != 0
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -126,6 +145,11 @@ cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cud
 
 // Whether the chain's last iterate (after `iters` iterations) carries a lo plane.
 bool ns_final_has_lo(int iters);
+
+// Whether the last iteration's update can write W (or the output) itself
+// (NsChainArgs::fin); otherwise the iterate stays in the workspace for the
+// separate last pass.
+bool ns_final_fused(int iters);
 
 // Runs the whole chain; the final iterate is left in X0 if the number of
 // iterations is even, else in X1.  Returns cudaErrorNotSupported when the

@@ -157,9 +157,27 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   na.iters = iters;
   na.status = status;
   na.timeout_ns = g_timeout_ns.load();
+  const bool fused = ns_final_fused(iters);
+  if (fused) {
+    // the last update's epilogue writes W (or the output) from its fp32 result
+    FinalStore& f = na.fin;
+    f.mode = ap.mode == 0 ? 1 : 2;
+    f.rows = v.rows;
+    f.cols = v.cols;
+    f.tall = v.rows > v.cols;
+    f.dtype = ap.w_dtype;
+    f.w_ptrs = ap.w_ptrs;
+    f.w_ld = ap.row_stride;
+    f.out_base = ap.out_base;
+    f.wd_mask = ap.wd_mask;
+    f.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
+    f.decay_on = ap.decay_on;
+    f.lr_scale = ap.lr_scale;
+  }
   e = run_ns_chain(na, st);
   if (e == cudaErrorNotSupported) return MUON_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MUON_ERR_CUDA;
+  if (fused) return MUON_OK;
 
   ap.X = (iters % 2 == 0) ? na.X0 : na.X1;
   ap.x_lo_off = L.lo_off;

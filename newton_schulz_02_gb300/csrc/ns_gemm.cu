@@ -82,7 +82,9 @@ constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kEpiWarps = 4;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
 
-enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2 };
+// kEpiFinal: the update of the last iteration, whose epilogue writes W (or
+// the output) instead of the iterate; it never carries a lo plane.
+enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2, kEpiFinal = 3 };
 
 template <int BN>
 struct Cfg {
@@ -112,6 +114,7 @@ struct GemmParams {
   const float* mscale;
   uint32_t* status;
   uint64_t timeout_ns;
+  FinalStore fin;   // update, last iteration: fused scale / decay / store
 };
 
 // Tile t -> (matrix, tile row, tile column).  For symmetric outputs only the
@@ -203,6 +206,142 @@ __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32])
   }
 }
 
+// ---- last iteration: W <- W*decay - lr_scale*O' fused into the update ---------
+// ("Muon 优化器" Algorithm 1, last line; the mask is RFC-0023 §方案 2).  The
+// epilogue holds O' in fp32 for 32 consecutive wide-orientation elements
+// (row, col0 .. col0+31) per lane.  W is read before the accumulator is
+// ready: the tile's W lines are prefetched into L2 when the tile starts and
+// each chunk's W is loaded into registers one chunk ahead, so the
+// read-modify-write adds no HBM latency to the epilogue.  Padding rows and
+// columns and skipped matrices are left alone.
+struct FinTile {
+  void* base;        // W (mode 1) or the matrix's dense output (mode 2); nullptr = skip
+  int64_t ld;
+  float decay;
+  int n_real, m_real;
+};
+
+__device__ __forceinline__ FinTile fin_tile(const FinalStore& f, int b) {
+  FinTile t;
+  t.n_real = f.tall ? f.cols : f.rows;
+  t.m_real = f.tall ? f.rows : f.cols;
+  const bool muon = (f.mode == 1);
+  const int esz = (f.dtype == MUON_BF16) ? 2 : 4;
+  t.base = f.skip[b] ? nullptr
+           : muon    ? f.w_ptrs[b]
+                     : static_cast<void*>(static_cast<char*>(f.out_base) +
+                                          static_cast<int64_t>(b) * f.rows * f.cols * esz);
+  t.ld = muon ? f.w_ld : f.cols;
+  t.decay = (muon && (f.wd_mask == nullptr || f.wd_mask[b])) ? f.decay_on : 1.f;
+  return t;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// L2 prefetch of the W the calling lane's chunks [c0, c0 + nch) will read.
+__device__ __forceinline__ void fin_prefetch(const FinalStore& f, const FinTile& t, int row,
+                                             int row0, int col_begin, int ncols, int lane) {
+  if (t.base == nullptr || f.mode != 1) return;
+  const int esz = (f.dtype == MUON_BF16) ? 2 : 4;
+  const char* base = static_cast<const char*>(t.base);
+  if (!f.tall) {
+    if (row >= t.n_real) return;
+    const int c_end = min(col_begin + ncols, t.m_real);
+    for (int j = col_begin; j < c_end; j += 128 / esz)
+      prefetch_l2(base + (static_cast<int64_t>(row) * t.ld + j) * esz);
+  } else {
+    if (row0 >= t.n_real) return;
+    // W[j][row0 .. row0+31]: one 64- or 128-byte segment per W row j
+    for (int j = col_begin + lane; j < col_begin + ncols; j += 32)
+      if (j < t.m_real) prefetch_l2(base + (static_cast<int64_t>(j) * t.ld + row0) * esz);
+  }
+}
+
+// W of one chunk into registers (raw bits; bf16 wide packs two per word).
+__device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, int row, int col0,
+                                         uint32_t (&w)[32]) {
+  if (t.base == nullptr || f.mode != 1 || row >= t.n_real) return;
+  const bool bf = (f.dtype == MUON_BF16);
+  if (!f.tall) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = col0 + 8 * k;
+      if (j >= t.m_real) continue;  // m_real is a multiple of 8
+      const int64_t off = static_cast<int64_t>(row) * t.ld + j;
+      if (bf) {
+        const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(t.base) + off);
+        w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+      } else {
+        const uint4* q = reinterpret_cast<const uint4*>(static_cast<const float*>(t.base) + off);
+        const uint4 u0 = q[0], u1 = q[1];
+        w[8 * k] = u0.x; w[8 * k + 1] = u0.y; w[8 * k + 2] = u0.z; w[8 * k + 3] = u0.w;
+        w[8 * k + 4] = u1.x; w[8 * k + 5] = u1.y; w[8 * k + 6] = u1.z; w[8 * k + 7] = u1.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int j = col0 + e;
+      if (j >= t.m_real) continue;
+      const int64_t off = static_cast<int64_t>(j) * t.ld + row;
+      w[e] = bf ? static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(
+                      static_cast<const __nv_bfloat16*>(t.base) + off))
+                : *reinterpret_cast<const uint32_t*>(static_cast<const float*>(t.base) + off);
+    }
+  }
+}
+
+__device__ __forceinline__ float fin_w(bool bf, bool tall, const uint32_t (&w)[32], int e) {
+  if (!bf) return __uint_as_float(w[e]);
+  // bf16 bits: packed pairs (wide) or one per word (tall)
+  const uint32_t h = tall ? (w[e] & 0xffffu) : ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu));
+  return __uint_as_float(h << 16);
+}
+
+__device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t, int row, int col0,
+                                          const float (&v)[32], const uint32_t (&w)[32]) {
+  if (t.base == nullptr || row >= t.n_real) return;
+  const bool muon = (f.mode == 1);
+  const bool bf = (f.dtype == MUON_BF16);
+  float o[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    o[e] = muon ? fmaf(-f.lr_scale, v[e], fin_w(bf, f.tall, w, e) * t.decay) : v[e];
+  if (!f.tall) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int j = col0 + 8 * k;
+      if (j >= t.m_real) continue;
+      const int64_t off = static_cast<int64_t>(row) * t.ld + j;
+      if (bf) {
+        uint4 u;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(o[8 * k + 2 * e], o[8 * k + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(t.base) + off) = u;
+      } else {
+        float4* q = reinterpret_cast<float4*>(static_cast<float*>(t.base) + off);
+        q[0] = make_float4(o[8 * k], o[8 * k + 1], o[8 * k + 2], o[8 * k + 3]);
+        q[1] = make_float4(o[8 * k + 4], o[8 * k + 5], o[8 * k + 6], o[8 * k + 7]);
+      }
+    }
+  } else {
+    // W[j][row]: the warp's 32 lanes store 32 consecutive elements of W row j
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int j = col0 + e;
+      if (j >= t.m_real) continue;
+      const int64_t off = static_cast<int64_t>(j) * t.ld + row;
+      if (bf)
+        static_cast<__nv_bfloat16*>(t.base)[off] = __float2bfloat16_rn(o[e]);
+      else
+        static_cast<float*>(t.base)[off] = o[e];
+    }
+  }
+}
+
 // Epilogue of one 128 x BN tile for the calling warp (TMEM lane quarter q,
 // rows tm*128 + q*32 + lane): waits for the accumulator (tfull_bar, parity),
 // applies the kernel's epilogue and stores.  The residual operand of the next
@@ -228,6 +367,14 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     load_raw4(aux_row + c_begin * 32, cur_h);
     if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
   }
+  constexpr bool kFin = (EPI == kEpiFinal);
+  FinTile ft{};
+  uint32_t w_cur[32], w_nxt[32];
+  if (kFin) {
+    ft = fin_tile(p.fin, b);
+    fin_prefetch(p.fin, ft, row, row0, tn * BN + c_begin * 32, kChunksPerWarp * 32, lane);
+    fin_load(p.fin, ft, row, tn * BN + c_begin * 32, w_cur);
+  }
   if (!mbar_wait_bounded(tfull_bar, parity, abort_flag, p.status, p.timeout_ns)) return false;
   tc_fence_after();
   float ms = 1.f;
@@ -240,6 +387,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     if (EPI != kEpiGram && i + 1 < kChunksPerWarp) {
       load_raw4(aux_row + (c + 1) * 32, nxt_h);
       if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
+      if (kFin) fin_load(p.fin, ft, row, tn * BN + (c + 1) * 32, w_nxt);
     }
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_row + c * 32, r);
@@ -272,7 +420,8 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
         }
       }
     }
-    if (EPI != kEpiUpdate && p.pdiag != nullptr && row >= col0 && row < col0 + 32) {
+    if ((EPI == kEpiGram || EPI == kEpiPoly) && p.pdiag != nullptr && row >= col0 &&
+        row < col0 + 32) {
       // the (a - 1) I shift; the diagonal's bf16 rounding residual is kept
       // in fp32 so that P's diagonal is exact to fp32 in the update
 #pragma unroll
@@ -282,6 +431,16 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
           p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
               v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
         }
+    }
+    if (kFin) {
+      fin_store(p.fin, ft, row, col0, v, w_cur);
+      if (i + 1 < kChunksPerWarp) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cur_h[k] = nxt_h[k];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) w_cur[e] = w_nxt[e];
+      }
+      continue;
     }
     __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
     uint4* dst = reinterpret_cast<uint4*>(drow);
@@ -721,6 +880,7 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
   }
 }
 
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -856,11 +1016,14 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
   return cudaGetLastError();
 }
 
+
 struct OperandMaps {
   CUtensorMap k128, kbn, mn, mn_lo;
 };
 
 }  // namespace
+
+bool ns_final_fused(int iters) { return iters > kLoIters; }
 
 bool ns_final_has_lo(int iters) { return iters < kLoIters; }
 
@@ -960,6 +1123,25 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.lo_out = it + 1 < kLoIters;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
+    const bool fin = (it + 1 == a.iters) && a.fin.mode != 0;
+    if (fin) {
+      // the last update writes W (or the output); it has no lo plane
+      u.fin = a.fin;
+      u.lo_in = false;
+      u.lo_out = false;
+      if (bn_up == 256 && pair && kUseTwoSm)
+        e = launch_gemm2<true, kEpiFinal, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+      else if (bn_up == 256 && pair)
+        e = launch_gemm<256, true, kEpiFinal, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+      else if (bn_up == 256)
+        e = launch_gemm<256, true, kEpiFinal, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+      else if (pair)
+        e = launch_gemm<128, true, kEpiFinal, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+      else
+        e = launch_gemm<128, true, kEpiFinal, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
     if (bn_up == 256 && pair && kUseTwoSm)
       e = launch_gemm2<true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
     else if (bn_up == 256 && pair)

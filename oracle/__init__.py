@@ -7,5 +7,5 @@ from .muon_ref import (  # noqa: F401
     SCALE_NONE, SCALE_SPECTRAL, SCALE_UNIT_RMS_NORM, STABLE_COEFFS, MuonHyper,
     bias_correct, decoupled_update, expand_stages, frobenius_normalize, group_by_shape,
     head_slices, lookahead_ema, lookahead_sgd, momentum_ema, momentum_sgd, muon_step,
-    newton_schulz, newton_schulz_literal, ns_iteration, update_scale,
+    newton_schulz, newton_schulz_literal, ns_iteration, row_blocks, update_scale,
 )

@@ -266,6 +266,17 @@ def head_slices(W: np.ndarray, n_heads: int, head_dim: int) -> list[np.ndarray]:
     return [W[:, h * head_dim:(h + 1) * head_dim] for h in range(n_heads)]
 
 
+def row_blocks(W: np.ndarray, parts: int) -> list[np.ndarray]:
+    """Sub-matrices of a weight stacked along rows, [parts*r, c] -> parts of
+    [r, c] (reading of split_linear_fc1, named in RFC-0023 §实施计划 SubTask S5: a fused
+    FC1 [gate; up] weight is orthogonalised as its separate blocks)."""
+    W = np.asarray(W)
+    if W.shape[0] % parts != 0:
+        raise ValueError("rows must split into equal parts")
+    r = W.shape[0] // parts
+    return [W[k * r:(k + 1) * r] for k in range(parts)]
+
+
 def group_by_shape(keys: Sequence[tuple], max_batch: int) -> tuple[list[int], int]:
     """Group tensors whose keys (shape, dtypes, view kind) are equal, in
     order of first appearance; each group of the same key is cut into chunks

@@ -264,6 +264,24 @@ def test_split_head_attention_weight(scale_mode):
         check_w(Wg[:, s], ref["W"], hp, ref["scale"], bf16=True)
 
 
+def test_split_linear_fc1_rows():
+    """Fused [gate; up] FC1 weight (2 x 512 rows, 384 columns, fp32 W):
+    each row block is orthogonalised on its own (fan_out = its rows)."""
+    W, G, M = workloads.random_case(60, 1024, 384, batch=1, w_dtype=torch.float32)
+    W, G, M = W[0], G[0], M[0]
+    W0, G0, M0 = f64(W), f64(G), f64(M)
+    Wd, Gd, Md = W.to(DEV), G.to(DEV), M.to(DEV)
+    for mode in ("spectral", "unit_rms_norm"):
+        Wp, Mp = f64(Wd), Md.cpu().numpy().astype(np.float64)
+        code, flags = step_once([m.Group.split_rows(Wd, Gd, Md, 2)], dict(scale_mode=mode))
+        assert code == m.MUON_OK and flags == 0
+        hp = hyper(scale_mode=mode)
+        for k, (w, g, mm) in enumerate(zip(oracle.row_blocks(Wp, 2), oracle.row_blocks(G0, 2),
+                                           oracle.row_blocks(Mp, 2))):
+            ref = oracle.muon_step(w, g, mm, hp)
+            check_w(f64(Wd[512 * k:512 * (k + 1)]), ref["W"], hp, ref["scale"], bf16=False)
+
+
 # ---------------------------------------------------------------------------
 # device status
 # ---------------------------------------------------------------------------

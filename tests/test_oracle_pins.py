@@ -298,6 +298,14 @@ def test_split_head_fan_rule():
         math.sqrt(128 / 4096), rel=1e-15)
 
 
+def test_row_blocks_are_contiguous_row_ranges():
+    W = np.arange(6 * 4, dtype=np.float64).reshape(6, 4)
+    gate, up = oracle.row_blocks(W, 2)
+    assert np.array_equal(gate, W[:3]) and np.array_equal(up, W[3:])
+    with pytest.raises(ValueError):
+        oracle.row_blocks(W, 4)
+
+
 def test_group_by_shape_golden():
     K0, K1, K2 = (1024, 1024, 0, 0, 0), (1024, 4096, 0, 0, 0), (8, 16, 0, 0, 0)
     keys = [K0, K1, K0, K0, K2, K1]
