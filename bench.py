@@ -9,7 +9,10 @@ step (sigma 1e-3, per-row scales log-uniform in [0.1, 10]), cycling through
 the 5 steps of grads; spectral scale, mu 0.95, lr 2.7e-4, wd 0.1.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload stack|single|heads]
+                    [--workload stack|single|heads|dense|moe|adamw]
+
+--workload adamw times the AdamW partition instead (muon_adamw_step over the
+dense 32-layer model's embedding, output head and norm scales: 1.05 B params).
 
 N > 1 runs one process per GPU (torchrun); each rank updates its own copy of
 the workload (matrices are independent units: weak scaling, no collective).
@@ -36,7 +39,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["stack", "single", "heads", "dense", "moe"],
+    ap.add_argument("--workload", choices=["stack", "single", "heads", "dense", "moe", "adamw"],
                     default="stack")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -490,9 +493,188 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# AdamW partition (muon_adamw_step)
+# ---------------------------------------------------------------------------
+ADAMW_METRIC = "AdamW-step params/s (AdamW partition of the dense 32-layer model)"
+ADAMW_DESC = dict(workload="adamw: dense 32-layer model's AdamW partition: embedding and head "
+                           "128256x4096, 65 norm scales of 4096", params=2 * 128256 * 4096 + 65 * 4096,
+                  w_dtype="bf16", g_dtype="bf16", moments="fp32", beta1=0.9, beta2=0.95,
+                  eps=1e-20, weight_decay=0.1, seed=5,
+                  l2="inputs larger than L2 (12.6 GB of W, G, m, v)")
+
+
+def adamw_oracle_sample(W, G, M, V, seconds: float):
+    """Oracle AdamW on consecutive 2^20-element slices of the embedding until
+    `seconds` have passed (host copies outside the timing)."""
+    import numpy as np
+    from oracle import adamw_ref
+    n = 1 << 20
+    flat = [x.view(-1) for x in (W, G, M, V)]
+    done = params = 0
+    spent = 0.0
+    while done < 1 or spent < seconds:
+        lo = (done * n) % (flat[0].numel() - n)
+        w, g, mm, vv = (x[lo:lo + n].float().cpu().numpy().astype(np.float64) for x in flat)
+        t0 = time.perf_counter()
+        adamw_ref.adamw_step(w, g, mm, vv, adamw_ref.AdamWHyper(t=3))
+        spent += time.perf_counter() - t0
+        done += 1
+        params += n
+    return params / spent, done, spent
+
+
+def run_adamw(args):
+    import torch
+    import torch.distributed as dist
+
+    import newton_schulz_02_gb300 as m
+    import workloads
+
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        torch.manual_seed(5)
+        n = 1 << 24
+        W = (torch.randn(n) * 0.02).to(torch.bfloat16)
+        G = (torch.randn(n) * 1e-3).to(torch.bfloat16)
+        M, V = torch.zeros(n), torch.zeros(n)
+        per = 120.0 / max(1, args.steps + args.warmup)
+        t0 = time.perf_counter()
+        params = units = 0
+        for _ in range(args.steps):
+            v, k, dt = adamw_oracle_sample(W, G, M, V, min(per, 10.0))
+            params += v * dt
+            units += k
+        dt = time.perf_counter() - t0
+        value = params / max(dt, 1e-9)
+        sample = f"{units} slices of 2^20 elements over {args.steps} steps (float64 NumPy oracle)"
+        print(json.dumps({"impl": "reference", "metric": ADAMW_METRIC, "value": value,
+                          "unit": "params/s", "n_gpus": args.gpus, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic", "config": ADAMW_DESC,
+                          "cpu_baseline": {"value": value, "unit": "params/s",
+                                           "cores": cpu_cores(), "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    m.load_library()
+    peaks, peak_src = load_peaks()
+    part = workloads.dense_adamw_partition(seed=5 + 1000 * rank, device=dev)
+    W, G, M, V = part["W"], part["G"], part["m"], part["v"]
+    groups = m.adamw_groups(W, G, M, V, wd_mask=part["wd_mask"])
+    P = int(sum(w.numel() for w in W))
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    t = 1
+    for _ in range(args.warmup):
+        m.muon_adamw_step(groups, m.adamw_hparams(t=t), flags)
+        t += 1
+    torch.cuda.synchronize()
+    m.muon_profile_reset()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            m.muon_adamw_step(groups, m.adamw_hparams(t=t), flags)
+            t += 1
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = start.elapsed_time(stop)
+    launches = int(sum(v["launches"] for v in m.muon_profile_query().values()))
+    if int(flags.item()) != 0:
+        raise RuntimeError(f"device flags {int(flags.item()):#x}")
+    prof_steps = max(1, min(args.steps, args.prof_steps))
+    m.muon_profile_reset()
+    m.muon_profile_enable(True)
+    for _ in range(prof_steps):
+        m.muon_adamw_step(groups, m.adamw_hparams(t=t), flags)
+        t += 1
+    torch.cuda.synchronize()
+    m.muon_profile_enable(False)
+    d = m.muon_profile_query()["adamw"]
+    ms = max_over_ranks(ms, world, dev)
+    value = job_value(args.steps, P, world, ms)
+    avg_s = d["total_ms"] / d["launches"] / 1e3
+    per_launch = d["alg_bytes"] / d["launches"]
+    achieved = per_launch / avg_s / 1e9
+    roof = {"kernel": "adamw", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "alg_bytes_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
+            "timing": f"event pair per launch, {prof_steps} profiled steps after the timed region",
+            "peak_source": f"{peak_src} copy"}
+
+    e2e = None
+    if args.e2e_steps > 0:
+        # pinned host gradients in, updated W out, every step
+        Gh = [g.cpu().pin_memory() for g in G]
+        Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
+        steps = max(1, min(args.e2e_steps, 5))
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for g, gh in zip(G, Gh):
+                g.copy_(gh, non_blocking=True)
+            m.muon_adamw_step(groups, m.adamw_hparams(t=t), flags)
+            t += 1
+            for w, wh in zip(W, Wh):
+                wh.copy_(w, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": job_value(steps, P, world, e_ms), "unit": "params/s",
+               "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in G)),
+               "d2h_bytes_per_step": int(sum(w.numel() * w.element_size() for w in W)),
+               "steps": steps, "path": "pinned host G -> device, muon_adamw_step, device W -> "
+                                        "pinned host"}
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    cpu_v, cpu_n, cpu_dt = adamw_oracle_sample(W[0], G[0], M[0], V[0], args.cpu_seconds)
+    desc = dict(ADAMW_DESC, parallelism=f"replicas x{world} (independent tensors, no collective)")
+    out = {"metric": ADAMW_METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded Gaussian weights and grads)", "config": desc,
+           "roofline": roof,
+           "kernels": {"adamw": {"launches": d["launches"], "total_ms": round(d["total_ms"], 4),
+                                 "share": 1.0, "gbs": round(achieved, 1),
+                                 "hbm_frac_of_measured": round(achieved / peaks["hbm_gbs"], 3)}},
+           "cpu_baseline": {"value": cpu_v, "unit": "params/s", "cores": cpu_cores(),
+                            "kind": "oracle",
+                            "sample": f"{cpu_n} slices of 2^20 embedding elements, one AdamW "
+                                      f"step each, float64 NumPy, {cpu_dt:.1f} s"},
+           "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
+           "peaks": dict(peaks, source=peak_src)}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     sys.path.insert(0, ROOT)
+    if args.workload == "adamw":
+        return run_adamw(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -246,6 +246,54 @@ muon_status_t newton_schulz_batched_noalloc(const void* x, muon_dtype_t xdt,
                                             muon_dtype_t odt, const muon_ns_schedule_t* schedule,
                                             uint32_t* device_flags, muon_stream_t stream);
 
+/* ---- AdamW partition ------------------------------------------------------
+ * The parameters that stay on AdamW next to Muon: embeddings, the output
+ * head, norm scales and other non-matrix tensors ("Muon 优化器" §3, whose V4
+ * settings are beta1 0.9, beta2 0.95, eps 1e-20, weight decay 0.1), with the
+ * per-tensor decay mask of "RFC-0023" §方案 2.  Per element, in fp32:
+ *
+ *   m <- beta1*m + (1 - beta1)*g
+ *   v <- beta2*v + (1 - beta2)*g^2
+ *   u  = (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+ *   W <- W*(1 - lr*wd*mask) - lr*u
+ *
+ * (the pages name AdamW without writing it out: this is Adam with bias
+ * correction and decoupled decay, eps outside the square root, the form of
+ * optax's adamw and PyTorch's AdamW). */
+
+/* `count` contiguous tensors of `numel` elements each (any shape).
+ * w_ptrs, g_ptrs, m_ptrs, v_ptrs: DEVICE arrays of `count` DEVICE pointers,
+ * each 16-byte aligned; W is w_dtype, G is g_dtype, m and v (first and second
+ * moments) are fp32; W, m and v are updated in place.  numel need not be a
+ * multiple of anything.  wd_mask: DEVICE [count] of 0/1 (1 = decay), NULL =
+ * all on. */
+typedef struct {
+  int count;
+  int64_t numel;
+  muon_dtype_t w_dtype, g_dtype;
+  void* const* w_ptrs;
+  const void* const* g_ptrs;
+  float* const* m_ptrs;
+  float* const* v_ptrs;
+  const uint8_t* wd_mask;
+} muon_adamw_group_t;
+
+/* t: steps taken including this one (>= 1).  0 <= beta1, beta2 < 1; eps >= 0. */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+  int64_t t;
+} muon_adamw_hparams_t;
+
+/* One AdamW step for every tensor of every group, on `stream`, in one
+ * kernel launch per 16 groups.  groups: host array [n_groups]; hparams: host.
+ * Needs no workspace.  device_flags: NULL, or a caller-owned device word
+ * (4-byte aligned) into which the kernel ORs MUON_FLAG_MISALIGNED when a
+ * pointer in a pointer array is not 16-byte aligned (that tensor is left
+ * untouched); the caller clears it.  Returns before the GPU work completes. */
+muon_status_t muon_adamw_step(const muon_adamw_group_t* groups, int n_groups,
+                              const muon_adamw_hparams_t* hparams, uint32_t* device_flags,
+                              muon_stream_t stream);
+
 /* Per-kernel statistics since the last muon_profile_reset.  Launches are
  * always counted.  With profiling on, the library records a CUDA event pair
  * on the launching stream around every kernel launch and total_ms sums their

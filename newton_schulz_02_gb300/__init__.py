@@ -77,6 +77,17 @@ class muon_kernel_stats_t(ctypes.Structure):
                 ("alg_flops", ctypes.c_double), ("alg_bytes", ctypes.c_double)]
 
 
+class muon_adamw_group_t(ctypes.Structure):
+    _fields_ = [("count", c_int), ("numel", c_int64), ("w_dtype", c_int), ("g_dtype", c_int),
+                ("w_ptrs", c_void_p), ("g_ptrs", c_void_p), ("m_ptrs", c_void_p),
+                ("v_ptrs", c_void_p), ("wd_mask", c_void_p)]
+
+
+class muon_adamw_hparams_t(ctypes.Structure):
+    _fields_ = [("lr", c_float), ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
+                ("weight_decay", c_float), ("t", c_int64)]
+
+
 # C prototypes: name -> (restype, argtypes)
 PROTOTYPES = {
     "muon_ns_hybrid_schedule": (c_int, [POINTER(muon_ns_schedule_t)]),
@@ -101,6 +112,8 @@ PROTOTYPES = {
     "muon_profile_reset": (c_int, []),
     "muon_profile_query": (c_int, [POINTER(muon_kernel_stats_t), c_int, POINTER(c_int)]),
     "muon_status_string": (c_char_p, [c_int]),
+    "muon_adamw_step": (c_int, [POINTER(muon_adamw_group_t), c_int, POINTER(muon_adamw_hparams_t),
+                                c_void_p, c_void_p]),
 }
 
 _lib = None
@@ -362,3 +375,70 @@ def muon_profile_query() -> dict:
     return {arr[i].name.decode(): dict(launches=arr[i].launches, total_ms=arr[i].total_ms,
                                        alg_flops=arr[i].alg_flops, alg_bytes=arr[i].alg_bytes)
             for i in range(min(n.value, 16))}
+
+
+# ---------------------------------------------------------------------------
+# AdamW partition
+# ---------------------------------------------------------------------------
+class AdamWGroup:
+    """Tensors of one element count and dtype pair (any shapes, contiguous):
+    the device arrays of device pointers muon_adamw_step takes."""
+
+    def __init__(self, W: Sequence[torch.Tensor], G: Sequence[torch.Tensor],
+                 m: Sequence[torch.Tensor], v: Sequence[torch.Tensor],
+                 wd_mask: Optional[Sequence[bool]] = None):
+        if not (len(W) == len(G) == len(m) == len(v) and len(W) > 0):
+            raise ValueError("W, G, m, v must be equally long and non-empty")
+        n = W[0].numel()
+        for t in list(W) + list(G) + list(m) + list(v):
+            if t.numel() != n or not t.is_contiguous():
+                raise ValueError("all tensors of a group need one element count and to be contiguous")
+        for t in list(m) + list(v):
+            if t.dtype != torch.float32:
+                raise ValueError("moments are fp32")
+        dev = W[0].device
+        self.tensors = (list(W), list(G), list(m), list(v))
+        self.ptrs = torch.tensor([[t.data_ptr() for t in x] for x in self.tensors],
+                                 dtype=torch.int64, device=dev)
+        self.mask = None
+        if wd_mask is not None:
+            self.mask = torch.tensor([1 if k else 0 for k in wd_mask], dtype=torch.uint8, device=dev)
+        stride = self.ptrs.stride(0) * 8
+        base = self.ptrs.data_ptr()
+        self.c = muon_adamw_group_t(len(W), n, _DT[W[0].dtype], _DT[G[0].dtype], base,
+                                    base + stride, base + 2 * stride, base + 3 * stride,
+                                    self.mask.data_ptr() if self.mask is not None else None)
+
+
+def adamw_groups(W, G, m, v, wd_mask=None) -> list:
+    """Group parallel lists of tensors by (element count, W dtype, G dtype), in
+    order of first appearance."""
+    keys, members = [], {}
+    for i, w in enumerate(W):
+        k = (w.numel(), w.dtype, G[i].dtype)
+        if k not in members:
+            keys.append(k)
+            members[k] = []
+        members[k].append(i)
+    out = []
+    for k in keys:
+        idx = members[k]
+        out.append(AdamWGroup([W[i] for i in idx], [G[i] for i in idx], [m[i] for i in idx],
+                              [v[i] for i in idx],
+                              None if wd_mask is None else [wd_mask[i] for i in idx]))
+    return out
+
+
+def adamw_hparams(lr=2.7e-4, beta1=0.9, beta2=0.95, eps=1e-20, weight_decay=0.1,
+                  t=1) -> muon_adamw_hparams_t:
+    return muon_adamw_hparams_t(float(lr), float(beta1), float(beta2), float(eps),
+                                float(weight_decay), int(t))
+
+
+def muon_adamw_step(groups: Sequence[AdamWGroup], hp: muon_adamw_hparams_t,
+                    flags: Optional[torch.Tensor] = None, stream=None) -> None:
+    """flags: optional int32 device tensor of one element (MUON_FLAG_* are ORed in)."""
+    arr = (muon_adamw_group_t * max(1, len(groups)))(*[g.c for g in groups])
+    _check(load_library().muon_adamw_step(arr, len(groups), ctypes.byref(hp),
+                                          flags.data_ptr() if flags is not None else None,
+                                          _stream(stream)), "muon_adamw_step")

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libmuon_gb300.so")
-SOURCES = ["muon_api.cu", "elementwise.cu", "ns_gemm.cu", "prof.cu", "noalloc.cu"]
+SOURCES = ["muon_api.cu", "elementwise.cu", "ns_gemm.cu", "prof.cu", "noalloc.cu", "adamw.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

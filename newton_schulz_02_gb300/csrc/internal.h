@@ -130,6 +130,7 @@ enum KernelKind : int {
   kKindUpdate,
   kKindApply,
   kKindTimeoutCheck,
+  kKindAdamW,
   kKindCount
 };
 void prof_begin(KernelKind k, cudaStream_t st);
@@ -141,6 +142,30 @@ int apply_parts(int rows, int cols);
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st);
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st);
 cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st);
+// ---- AdamW partition (adamw.cu) ----
+constexpr int kAdamWMaxGroups = 16;  // groups per launch (kernel-parameter table)
+
+struct AdamWGroupArgs {
+  int count;                 // tensors in the group
+  int64_t numel;             // elements per tensor
+  int64_t chunks_per_tensor; // filled by launch_adamw
+  int w_dtype, g_dtype;
+  void* const* w_ptrs;       // device arrays [count] of device pointers
+  const void* const* g_ptrs;
+  float* const* m_ptrs;
+  float* const* v_ptrs;
+  const uint8_t* wd_mask;    // device [count] or nullptr (all on)
+};
+
+struct AdamWScalars {
+  float lr, beta1, omb1, beta2, omb2, eps;
+  float c1, c2;              // 1/(1 - beta1^t), 1/(1 - beta2^t)
+  float decay_on;            // 1 - lr*wd
+};
+
+cudaError_t launch_adamw(AdamWGroupArgs* groups, int n_groups, const AdamWScalars& s,
+                         uint32_t* flags, cudaStream_t st);
+
 cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 
 // Whether the chain's last iterate (after `iters` iterations) carries a lo plane.

@@ -467,6 +467,55 @@ muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
       launch_wait_timeout_check(static_cast<uint32_t*>(workspace), timeout_ns, st));
 }
 
+muon_status_t muon_adamw_step(const muon_adamw_group_t* groups, int n_groups,
+                              const muon_adamw_hparams_t* hp, uint32_t* device_flags,
+                              muon_stream_t stream) {
+  if (hp == nullptr || n_groups < 0 || (n_groups > 0 && groups == nullptr))
+    return MUON_ERR_INVALID_ARG;
+  if (hp->t < 1 || !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f))
+    return MUON_ERR_INVALID_ARG;
+  if (!(hp->eps >= 0.f) || !std::isfinite(hp->eps) || !std::isfinite(hp->lr) ||
+      !std::isfinite(hp->weight_decay))
+    return MUON_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(device_flags) & 3u) != 0) return MUON_ERR_MISALIGNED;
+  std::vector<AdamWGroupArgs> args;
+  args.reserve(static_cast<size_t>(n_groups));
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_adamw_group_t& g = groups[i];
+    if (g.count < 0 || g.numel < 0) return MUON_ERR_INVALID_ARG;
+    if (!valid_dtype(g.w_dtype) || !valid_dtype(g.g_dtype)) return MUON_ERR_INVALID_ARG;
+    if (g.count == 0 || g.numel == 0) continue;
+    if (g.w_ptrs == nullptr || g.g_ptrs == nullptr || g.m_ptrs == nullptr || g.v_ptrs == nullptr)
+      return MUON_ERR_INVALID_ARG;
+    AdamWGroupArgs a{};
+    a.count = g.count;
+    a.numel = g.numel;
+    a.w_dtype = g.w_dtype;
+    a.g_dtype = g.g_dtype;
+    a.w_ptrs = g.w_ptrs;
+    a.g_ptrs = g.g_ptrs;
+    a.m_ptrs = g.m_ptrs;
+    a.v_ptrs = g.v_ptrs;
+    a.wd_mask = g.wd_mask;
+    args.push_back(a);
+  }
+  if (args.empty()) return MUON_OK;
+  // bias corrections and coefficients in double from the fp32 values given
+  const double b1 = hp->beta1, b2 = hp->beta2, t = static_cast<double>(hp->t);
+  AdamWScalars sc{};
+  sc.lr = hp->lr;
+  sc.beta1 = hp->beta1;
+  sc.beta2 = hp->beta2;
+  sc.omb1 = static_cast<float>(1.0 - b1);
+  sc.omb2 = static_cast<float>(1.0 - b2);
+  sc.eps = hp->eps;
+  sc.c1 = static_cast<float>(1.0 / (1.0 - std::pow(b1, t)));
+  sc.c2 = static_cast<float>(1.0 / (1.0 - std::pow(b2, t)));
+  sc.decay_on = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+  return cuda_status(launch_adamw(args.data(), static_cast<int>(args.size()), sc, device_flags,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char* muon_status_string(muon_status_t s) {
   switch (s) {
     case MUON_OK: return "MUON_OK";

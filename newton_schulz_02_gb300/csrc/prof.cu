@@ -26,7 +26,7 @@ struct Pending {
 };
 
 const char* const kNames[kKindCount] = {"prepare", "finalize_norm", "ns_gram", "ns_poly",
-                                        "ns_update", "apply", "timeout_check"};
+                                        "ns_update", "apply", "timeout_check", "adamw"};
 
 std::mutex g_mu;
 bool g_timing = false;

@@ -51,7 +51,9 @@ def test_struct_layouts_match_c(tmp_path):
         "#define P(T) printf(#T \" %zu\\n\", sizeof(T));\n"
         "#define O(T,f) printf(#T \".\" #f \" %zu\\n\", offsetof(T,f));\n"
         "int main(void){P(muon_ns_stage_t)P(muon_ns_schedule_t)P(muon_view_t)P(muon_group_t)"
-        "P(muon_hparams_t)P(muon_tensor_desc_t)"
+        "P(muon_hparams_t)P(muon_tensor_desc_t)P(muon_adamw_group_t)P(muon_adamw_hparams_t)"
+        "O(muon_adamw_group_t,numel)O(muon_adamw_group_t,w_ptrs)O(muon_adamw_group_t,wd_mask)"
+        "O(muon_adamw_hparams_t,weight_decay)O(muon_adamw_hparams_t,t)"
         "O(muon_group_t,view)O(muon_group_t,w_ptrs)O(muon_group_t,wd_mask)"
         "O(muon_hparams_t,t)O(muon_hparams_t,lr)O(muon_view_t,row_stride)"
         "O(muon_view_t,fan_out_axis)O(muon_tensor_desc_t,w_dtype)"
@@ -61,7 +63,8 @@ def test_struct_layouts_match_c(tmp_path):
                            "-o", str(exe)])
     got = dict(line.split() for line in subprocess.check_output([str(exe)], text=True).splitlines())
     for name in ["muon_ns_stage_t", "muon_ns_schedule_t", "muon_view_t", "muon_group_t",
-                 "muon_hparams_t", "muon_tensor_desc_t"]:
+                 "muon_hparams_t", "muon_tensor_desc_t", "muon_adamw_group_t",
+                 "muon_adamw_hparams_t"]:
         assert int(got[name]) == ctypes.sizeof(getattr(m, name)), name
     for key, val in got.items():
         if "." in key:
@@ -182,6 +185,32 @@ def test_step_rejects_before_enqueue(lib):
     L = m.load_library()
     assert L.muon_step_batched(None, 1, ctypes.byref(hp), None, 0x100000, need, None) == \
         m.MUON_ERR_INVALID_ARG
+
+
+def test_adamw_rejects_before_enqueue(lib):
+    """Host-detectable AdamW errors return before any CUDA call (no GPU here)."""
+    L = m.load_library()
+    g = m.muon_adamw_group_t(2, 100, m.MUON_BF16, m.MUON_BF16, 0x1000, 0x2000, 0x3000, 0x4000, None)
+    arr = (m.muon_adamw_group_t * 1)(g)
+    call = lambda a, n, hp, flags=None: L.muon_adamw_step(a, n, ctypes.byref(hp), flags, None)
+    hp = m.adamw_hparams()
+    assert call(arr, 1, m.adamw_hparams(t=0)) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, 1, m.adamw_hparams(beta1=1.0)) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, 1, m.adamw_hparams(beta2=-0.1)) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, 1, m.adamw_hparams(eps=-1e-8)) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, 1, m.adamw_hparams(lr=float("nan"))) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, 1, hp, 0x1002) == m.MUON_ERR_MISALIGNED
+    assert call(None, 1, hp) == m.MUON_ERR_INVALID_ARG
+    assert call(arr, -1, hp) == m.MUON_ERR_INVALID_ARG
+    for bad in (m.muon_adamw_group_t(-1, 100, 0, 0, 0x1000, 0x2000, 0x3000, 0x4000, None),
+                m.muon_adamw_group_t(2, -5, 0, 0, 0x1000, 0x2000, 0x3000, 0x4000, None),
+                m.muon_adamw_group_t(2, 100, 9, 0, 0x1000, 0x2000, 0x3000, 0x4000, None),
+                m.muon_adamw_group_t(2, 100, 0, 0, 0x1000, None, 0x3000, 0x4000, None)):
+        assert call((m.muon_adamw_group_t * 1)(bad), 1, hp) == m.MUON_ERR_INVALID_ARG
+    # empty groups enqueue nothing
+    empty = m.muon_adamw_group_t(0, 100, 0, 0, None, None, None, None, None)
+    assert call((m.muon_adamw_group_t * 1)(empty), 1, hp) == m.MUON_OK
+    assert call(arr, 0, hp) == m.MUON_OK
 
 
 def test_newton_schulz_rejects_before_enqueue(lib):

@@ -16,6 +16,8 @@ measured on:
            Gaussian grads sigma 1e-3 plus rank-8 spikes; seed 3
   moe      256 experts x {up 2048x7168, down 7168x2048}, Student-t (nu=3)
            grads scaled 1e-3; seed 4
+  adamw    the dense model's AdamW partition (embedding and head 128256 x 4096,
+           65 norm scales of 4096), Gaussian grads sigma 1e-3; seed 5
 
 A rank-k spike is U diag(s) V^T with U, V orthonormalised Gaussian columns and
 equal s chosen so that its Frobenius norm is 10x the noise's.  Small and large
@@ -185,3 +187,35 @@ def moe_experts(seed: int = 4, experts: int = 256, device="cuda", nu: int = 3,
         out[name] = (W, G, torch.zeros(experts, r, c, device=device))
         del z, chi2
     return out
+
+
+# ---------------------------------------------------------------------------
+# AdamW partition of the dense 32-layer model (hidden 4096): token embedding
+# and output head 128256 x 4096, two RMSNorm scales per layer plus the final
+# one (65 x 4096).  Drawn on the device.
+# ---------------------------------------------------------------------------
+VOCAB = 128256
+HIDDEN = 4096
+
+
+def dense_adamw_partition(seed: int = 5, layers: int = 32, device="cuda",
+                          vocab: int = VOCAB, hidden: int = HIDDEN) -> dict:
+    """{W, G, m, v: lists of tensors, wd_mask, names}.  W bf16: embedding and
+    head ~ N(0, 0.02^2), norm scales 1 + N(0, 0.02^2); G bf16 ~ N(0, 1e-3^2);
+    fp32 moments start at zero.  Decay on for the embedding and head, off for
+    the norm scales (the norm-parameter flag off)."""
+    gen = _device_gen(device, seed)
+    names = ["embed", "head"] + [f"norm{i}" for i in range(2 * layers + 1)]
+    W, G, M, V, mask = [], [], [], [], []
+    for nm in names:
+        shape = (vocab, hidden) if nm in ("embed", "head") else (hidden,)
+        w = torch.randn(shape, generator=gen, device=device) * W_STD
+        if nm.startswith("norm"):
+            w += 1.0
+        W.append(w.to(torch.bfloat16))
+        G.append((torch.randn(shape, generator=gen, device=device) * G_STD).to(torch.bfloat16))
+        M.append(torch.zeros(shape, device=device))
+        V.append(torch.zeros(shape, device=device))
+        mask.append(not nm.startswith("norm"))
+        del w
+    return {"W": W, "G": G, "m": M, "v": V, "wd_mask": mask, "names": names}
