@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--prof-steps", type=int, default=50)
+    ap.add_argument("--prec", choices=["bf16", "x3"], default="bf16",
+                    help="Newton–Schulz precision: bf16 (default) or split-bf16 (MUON_NS_BF16X3)")
     return ap.parse_args()
 
 
@@ -336,7 +338,11 @@ def run_ours(args):
         groups = make_groups(m, wl, Wd, Md, Gd)
         P = n_params(wl)
     hp = m.hparams()
-    ws = m.workspace(m.muon_step_workspace_size(groups[0]), device=dev)
+    sched = None
+    if args.prec == "x3":
+        sched = m.muon_ns_hybrid_schedule()
+        sched.prec = m.MUON_NS_BF16X3
+    ws = m.workspace(m.muon_step_workspace_size(groups[0], sched), device=dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -344,7 +350,7 @@ def run_ours(args):
             dist.barrier()
 
     for i in range(args.warmup):
-        m.muon_step_batched(groups[i % len(groups)], hp, ws)
+        m.muon_step_batched(groups[i % len(groups)], hp, ws, sched)
     code, flags = m.muon_get_status(ws)
     if code != m.MUON_OK or flags:
         raise RuntimeError(f"device status {code} flags {flags:#x} after warm-up")
@@ -358,7 +364,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            m.muon_step_batched(groups[i % len(groups)], hp, ws)
+            m.muon_step_batched(groups[i % len(groups)], hp, ws, sched)
         stop.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -374,7 +380,7 @@ def run_ours(args):
     m.muon_profile_enable(True)
     torch.cuda.synchronize()
     for i in range(prof_steps):
-        m.muon_step_batched(groups[i % len(groups)], hp, ws)
+        m.muon_step_batched(groups[i % len(groups)], hp, ws, sched)
     torch.cuda.synchronize()
     m.muon_profile_enable(False)
     prof = m.muon_profile_query()
@@ -431,7 +437,7 @@ def run_ours(args):
         flags_h = []
         for i in range(2):
             Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
-            m.muon_step_batched(eg, hp, ws)
+            m.muon_step_batched(eg, hp, ws, sched)
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
@@ -439,7 +445,7 @@ def run_ours(args):
         e0.record(stream)
         for i in range(args.e2e_steps):
             Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
-            m.muon_step_batched(eg, hp, ws)
+            m.muon_step_batched(eg, hp, ws, sched)
             Wh.copy_(Wd, non_blocking=True)
             flags_h.append(m.muon_get_status(ws))
         e1.record(stream)
@@ -468,6 +474,8 @@ def run_ours(args):
         rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
     clocks = clk.summary()
     desc = dict(wl["desc"])
+    desc["ns_precision"] = {"bf16": "bf16 (MUON_NS_BF16)",
+                            "x3": "split-bf16 (MUON_NS_BF16X3, three products per GEMM)"}[args.prec]
     desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
                 l2={"stack": "inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M "
                              "+ 768 MiB workspace",

@@ -82,11 +82,22 @@ typedef enum {
   MUON_SCALE_NONE = 2
 } muon_scale_mode_t;
 
-/* Precision of the Newton–Schulz chain: bf16 tensor-core operands with fp32
- * accumulation and fp32 epilogues; X X^T and the polynomial are stored in
- * bf16, the iterate as a bf16 value plus its bf16 rounding residual (about 16
- * significant bits).  MUON_NS_TF32 is reserved (returns MUON_ERR_UNSUPPORTED). */
-typedef enum { MUON_NS_BF16 = 0, MUON_NS_TF32 = 1 } muon_ns_precision_t;
+/* Precision of the Newton–Schulz chain (the pages fix none; "RFC-0023" §风险
+ * contrasts the float64 reference with bf16).  Every kind uses bf16
+ * tensor-core operands with fp32 accumulation and fp32 epilogues.
+ *  MUON_NS_BF16:   X X^T and the polynomial stored in bf16 (the polynomial's
+ *                  diagonal keeps an fp32 residual), the iterate as bf16 plus
+ *                  its bf16 rounding residual in the first iterations;
+ *                  relative error about 5e-3 against float64.
+ *  MUON_NS_BF16X3: split-bf16: X, X X^T and the polynomial all stored as
+ *                  hi + lo bf16 planes (about 16 significant bits), every
+ *                  product the three-term sum A_hi B_hi + A_hi B_lo + A_lo B_hi;
+ *                  relative error about 1e-5 for three times the tensor-core
+ *                  work and twice the workspace for X X^T and the polynomial.
+ *  MUON_NS_TF32:   reserved (returns MUON_ERR_UNSUPPORTED): one-pass TF32
+ *                  products, emulated, miss a 1e-3 relative bound on
+ *                  gradients with a low-rank spike. */
+typedef enum { MUON_NS_BF16 = 0, MUON_NS_TF32 = 1, MUON_NS_BF16X3 = 2 } muon_ns_precision_t;
 
 /* `steps` iterations of X <- a X + b (X X^T) X + c (X X^T)^2 X. */
 typedef struct {

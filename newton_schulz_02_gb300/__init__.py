@@ -33,7 +33,7 @@ MUON_FLAG_MISALIGNED = 0x4
 MUON_BF16, MUON_F32 = 0, 1
 MUON_NESTEROV_SGD, MUON_NESTEROV_EMA = 0, 1
 MUON_SCALE_SPECTRAL, MUON_SCALE_UNIT_RMS_NORM, MUON_SCALE_NONE = 0, 1, 2
-MUON_NS_BF16, MUON_NS_TF32 = 0, 1
+MUON_NS_BF16, MUON_NS_TF32, MUON_NS_BF16X3 = 0, 1, 2
 
 _DT = {torch.bfloat16: MUON_BF16, torch.float32: MUON_F32}
 _SCALE = {"spectral": MUON_SCALE_SPECTRAL, "unit_rms_norm": MUON_SCALE_UNIT_RMS_NORM,

@@ -116,6 +116,8 @@ struct NsChainArgs {
   const float* inv_s;   // folded into the first iteration; nullptr = no normalisation
   const float* coeffs;  // host [iters][3]
   int iters;
+  int x3;               // split-bf16 precision: S and P carry lo planes at +sq_lo_off
+  int64_t sq_lo_off;
   FinalStore fin;       // fused into the last iteration when fin.mode != 0
   uint32_t* status;
   uint64_t timeout_ns;
@@ -169,12 +171,12 @@ cudaError_t launch_adamw(AdamWGroupArgs* groups, int n_groups, const AdamWScalar
 cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
 
 // Whether the chain's last iterate (after `iters` iterations) carries a lo plane.
-bool ns_final_has_lo(int iters);
+bool ns_final_has_lo(int iters, bool x3);
 
 // Whether the last iteration's update can write W (or the output) itself
 // (NsChainArgs::fin); otherwise the iterate stays in the workspace for the
 // separate last pass.
-bool ns_final_fused(int iters);
+bool ns_final_fused(int iters, bool x3);
 
 // Runs the whole chain; the final iterate is left in X0 if the number of
 // iterations is even, else in X1.  Returns cudaErrorNotSupported when the

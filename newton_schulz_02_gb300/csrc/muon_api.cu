@@ -43,11 +43,12 @@ int dsize(int d) { return d == MUON_BF16 ? 2 : 4; }
 
 struct Layout {
   int n_pad = 0, m_pad = 0, parts = 0;
-  int64_t lo_off = 0;  // elements from an iterate's hi plane to its lo plane
+  int64_t lo_off = 0;     // elements from an iterate's hi plane to its lo plane
+  int64_t sq_lo_off = 0;  // split-bf16: from S's (P's) hi plane to its lo plane
   size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
 };
 
-Layout layout_for(int batch, int rows, int cols) {
+Layout layout_for(int batch, int rows, int cols, bool x3) {
   Layout L;
   const int n = rows < cols ? rows : cols, m = rows < cols ? cols : rows;
   L.n_pad = static_cast<int>(round_up(n, kPad));
@@ -60,8 +61,10 @@ Layout layout_for(int batch, int rows, int cols) {
   // each iterate: hi plane, then lo plane (lo_off = batch*n_pad*m_pad elements)
   L.x0 = off; off += 2 * align256(xb);
   L.x1 = off; off += 2 * align256(xb);
-  L.a = off; off += align256(sb);
-  L.b = off; off += align256(sb);
+  // S and P: hi plane (and, in the split-bf16 precision, a lo plane after it)
+  L.sq_lo_off = static_cast<int64_t>(align256(sb) / 2);
+  L.a = off; off += (x3 ? 2 : 1) * align256(sb);
+  L.b = off; off += (x3 ? 2 : 1) * align256(sb);
   L.pdiag = off; off += align256(static_cast<size_t>(batch) * L.n_pad * 4);
   L.partials = off; off += align256(static_cast<size_t>(batch) * L.parts * 4);
   L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
@@ -80,14 +83,14 @@ muon_status_t check_view(const muon_view_t& v) {
 }
 
 muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* coeffs,
-                              int* normalize) {
+                              int* normalize, bool* x3) {
   muon_ns_schedule_t def;
   if (s == nullptr) {
     muon_ns_hybrid_schedule(&def);
     s = &def;
   }
   if (s->prec == MUON_NS_TF32) return MUON_ERR_UNSUPPORTED;
-  if (s->prec != MUON_NS_BF16) return MUON_ERR_INVALID_ARG;
+  if (s->prec != MUON_NS_BF16 && s->prec != MUON_NS_BF16X3) return MUON_ERR_INVALID_ARG;
   if (s->n_stages < 0 || (s->n_stages > 0 && s->stages == nullptr)) return MUON_ERR_INVALID_ARG;
   if (s->normalize != 0 && s->normalize != 1) return MUON_ERR_INVALID_ARG;
   coeffs->clear();
@@ -103,6 +106,7 @@ muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* c
     }
   }
   *normalize = s->normalize;
+  *x3 = (s->prec == MUON_NS_BF16X3);
   return MUON_OK;
 }
 
@@ -125,8 +129,8 @@ muon_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MUON_OK : M
 
 // Shared tail of both entry points: norm, NS chain, last pass.
 muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_view_t& v,
-                             const std::vector<float>& coeffs, int normalize, ApplyArgs ap,
-                             cudaStream_t st) {
+                             const std::vector<float>& coeffs, int normalize, bool x3,
+                             ApplyArgs ap, cudaStream_t st) {
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   FinalizeArgs fa{};
   fa.batch = batch;
@@ -157,7 +161,9 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   na.iters = iters;
   na.status = status;
   na.timeout_ns = g_timeout_ns.load();
-  const bool fused = ns_final_fused(iters);
+  na.x3 = x3 ? 1 : 0;
+  na.sq_lo_off = L.sq_lo_off;
+  const bool fused = ns_final_fused(iters, x3);
   if (fused) {
     // the last update's epilogue writes W (or the output) from its fp32 result
     FinalStore& f = na.fin;
@@ -181,7 +187,7 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
 
   ap.X = (iters % 2 == 0) ? na.X0 : na.X1;
   ap.x_lo_off = L.lo_off;
-  ap.has_lo = ns_final_has_lo(iters) ? 1 : 0;
+  ap.has_lo = ns_final_has_lo(iters, x3) ? 1 : 0;
   ap.n_pad = L.n_pad;
   ap.m_pad = L.m_pad;
   ap.tall = v.rows > v.cols;
@@ -248,14 +254,15 @@ muon_status_t muon_step_workspace_size(const muon_group_t* groups, int n_groups,
     return MUON_ERR_INVALID_ARG;
   std::vector<float> coeffs;
   int normalize = 1;
-  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize);
+  bool x3 = false;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
   size_t need = kHeaderBytes;
   for (int i = 0; i < n_groups; ++i) {
     if (groups[i].batch < 1) return MUON_ERR_INVALID_ARG;
     s = check_view(groups[i].view);
     if (s != MUON_OK) return s;
-    const Layout L = layout_for(groups[i].batch, groups[i].view.rows, groups[i].view.cols);
+    const Layout L = layout_for(groups[i].batch, groups[i].view.rows, groups[i].view.cols, x3);
     if (L.total > need) need = L.total;
   }
   *bytes = need;
@@ -279,7 +286,8 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
     return MUON_ERR_INVALID_ARG;
   std::vector<float> coeffs;
   int normalize = 1;
-  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize);
+  bool x3 = false;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
   for (int i = 0; i < n_groups; ++i) {
     const muon_group_t& g = groups[i];
@@ -314,7 +322,7 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
 
   for (int i = 0; i < n_groups; ++i) {
     const muon_group_t& g = groups[i];
-    const Layout L = layout_for(g.batch, g.view.rows, g.view.cols);
+    const Layout L = layout_for(g.batch, g.view.rows, g.view.cols, x3);
     if (cudaMemsetAsync(ws + L.skip, 0, static_cast<size_t>(g.batch), st) != cudaSuccess)
       return MUON_ERR_CUDA;
     PrepareArgs pa{};
@@ -355,7 +363,7 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
     ap.wd_mask = g.wd_mask;
     ap.decay_on = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
     ap.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-    s = run_group_tail(L, ws, g.batch, g.view, coeffs, normalize, ap, st);
+    s = run_group_tail(L, ws, g.batch, g.view, coeffs, normalize, x3, ap, st);
     if (s != MUON_OK) return s;
   }
   return MUON_OK;
@@ -368,9 +376,10 @@ muon_status_t newton_schulz_workspace_size(const muon_view_t* view, int batch,
   if (s != MUON_OK) return s;
   std::vector<float> coeffs;
   int normalize = 1;
-  s = expand_schedule(schedule, &coeffs, &normalize);
+  bool x3 = false;
+  s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
-  *bytes = layout_for(batch, view->rows, view->cols).total;
+  *bytes = layout_for(batch, view->rows, view->cols, x3).total;
   return MUON_OK;
 }
 
@@ -397,9 +406,10 @@ muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_
   }
   std::vector<float> coeffs;
   int normalize = 1;
-  s = expand_schedule(schedule, &coeffs, &normalize);
+  bool x3 = false;
+  s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
-  const Layout L = layout_for(batch, view->rows, view->cols);
+  const Layout L = layout_for(batch, view->rows, view->cols, x3);
   s = check_workspace(workspace, workspace_bytes, L.total);
   if (s != MUON_OK) return s;
 
@@ -436,7 +446,7 @@ muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_
   ap.mode = 1;
   ap.w_dtype = odt;
   ap.out_base = out;
-  return run_group_tail(L, ws, batch, *view, coeffs, normalize, ap, st);
+  return run_group_tail(L, ws, batch, *view, coeffs, normalize, x3, ap, st);
 }
 
 muon_status_t muon_get_status(const void* workspace, muon_stream_t stream, uint32_t* flags) {

@@ -48,6 +48,13 @@
 // iterations costs little; written as a X + (b S + c S^2) X, converged
 // directions would cancel 3.44 X against -2.74 X and amplify the dropped
 // residual about ninefold.
+//
+// Split-bf16 precision (kEpiX3, MUON_NS_BF16X3): S, P and X are all stored
+// as hi + lo planes and every GEMM runs one K-loop over three plane pairs,
+// A_hi B_hi + A_hi B_lo + A_lo B_hi, which keeps about 16 significant bits
+// throughout.  With that precision the shift buys nothing and costs digits
+// when a is small (X + (S^2 - I) X cancels for a = 0), so the update is
+// evaluated as written, X' = a X + (b S + c S^2) X.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -84,7 +91,12 @@ constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue 
 
 // kEpiFinal: the update of the last iteration, whose epilogue writes W (or
 // the output) instead of the iterate; it never carries a lo plane.
-enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2, kEpiFinal = 3 };
+// kEpiX3 (or-ed into Gram / Poly / Update): the split-bf16 precision, in
+// which S, P and X are all stored as hi + lo planes and every product is the
+// three-term sum A_hi B_hi + A_hi B_lo + A_lo B_hi.
+enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2, kEpiFinal = 3, kEpiX3 = 4 };
+__host__ __device__ constexpr int epi_kind(int e) { return e & 3; }
+__host__ __device__ constexpr bool epi_x3(int e) { return (e & kEpiX3) != 0; }
 
 template <int BN>
 struct Cfg {
@@ -103,11 +115,13 @@ struct GemmParams {
   int64_t out_ld, out_bstride;
   const __nv_bfloat16* aux;
   int64_t aux_ld, aux_bstride;
-  int64_t lo_off;  // update: lo planes of aux and out at +lo_off elements
-  int lo_in, lo_out;  // update: read aux's lo plane / write out's lo plane
+  int64_t lo_off;  // lo planes of aux and out at +lo_off elements
+  int lo_in, lo_out;  // update (any kind with kEpiX3): read aux's lo plane / write out's lo plane
   float ca, cb, cc;
   float cd;         // added on the diagonal (Gram when c == 0, Poly): a - 1
-  int kplanes;      // update: 1 = B from hi; 2 = K-loop over hi then lo (tmB2)
+  int kplanes;      // K-loop over 1..3 operand planes; plane p reads A's lo plane
+  int a_lo_mask;    // (tmA2) if bit p of a_lo_mask is set, else its hi plane
+  int b_lo_mask;    // (tmA), and likewise B from tmB2 / tmB
   float* pdiag;     // Gram (c == 0) / Poly: fp32 rounding residual of P's diagonal, [batch][n]
   const float* pdiag_in;  // update: that residual, added back as d_row * X
   int64_t pdiag_bstride;
@@ -356,18 +370,22 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
   const int row0 = tm * kBM + q * 32;
   const int row = row0 + lane;
   const bool mirror = SYM && (tn > tm / (BN / kBM));
+  constexpr int K = epi_kind(EPI);
+  constexpr bool kX3 = epi_x3(EPI);
   const __nv_bfloat16* aux_row =
-      (EPI == kEpiGram) ? nullptr
+      (K == kEpiGram) ? nullptr
                         : p.aux + static_cast<int64_t>(b) * p.aux_bstride +
                               static_cast<int64_t>(row) * p.aux_ld + tn * BN;
   uint4 cur_h[4], cur_l[4], nxt_h[4], nxt_l[4];
-  const bool lo_in = (EPI == kEpiUpdate) && p.lo_in;
-  const bool lo_out = (EPI == kEpiUpdate) && p.lo_out;
-  if (EPI != kEpiGram) {
+  // lo planes: the update of the bf16 precision (runtime flags), every kind
+  // of the split-bf16 precision except the Gram's input
+  const bool lo_in = (K == kEpiUpdate || (kX3 && K == kEpiPoly)) && p.lo_in;
+  const bool lo_out = (K == kEpiUpdate || (kX3 && K != kEpiFinal)) && p.lo_out;
+  if (K != kEpiGram) {
     load_raw4(aux_row + c_begin * 32, cur_h);
     if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
   }
-  constexpr bool kFin = (EPI == kEpiFinal);
+  constexpr bool kFin = (K == kEpiFinal);
   FinTile ft{};
   uint32_t w_cur[32], w_nxt[32];
   if (kFin) {
@@ -384,7 +402,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
 #pragma unroll 1
   for (int i = 0; i < kChunksPerWarp; ++i) {
     const int c = c_begin + i;
-    if (EPI != kEpiGram && i + 1 < kChunksPerWarp) {
+    if (K != kEpiGram && i + 1 < kChunksPerWarp) {
       load_raw4(aux_row + (c + 1) * 32, nxt_h);
       if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
       if (kFin) fin_load(p.fin, ft, row, tn * BN + (c + 1) * 32, w_nxt);
@@ -394,14 +412,20 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     tmem_ld_wait(r);
     const int col0 = tn * BN + c * 32;
     float v[32];
-    if (EPI == kEpiGram) {
+    if (K == kEpiGram) {
       const float s2 = ms * ms * p.cb;
 #pragma unroll
       for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(r[e]) * s2;
     } else {
       float x[32];
       unpack_raw4(cur_h, x);
-      if (EPI == kEpiPoly) {
+      if (K == kEpiPoly) {
+        if (kX3 && lo_in) {
+          float xl[32];
+          unpack_raw4(cur_l, xl);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] += xl[e];
+        }
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = fmaf(p.cc, __uint_as_float(r[e]), p.cb * x[e]);
       } else {
@@ -412,15 +436,23 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
 #pragma unroll
           for (int e = 0; e < 32; ++e) xl[e] = 0.f;
         }
-        const float d = p.pdiag_in[static_cast<int64_t>(b) * p.pdiag_bstride + row];
+        if (kX3) {
+          // split-bf16: P = bS + cS^2 carries no shift, X' = a X + P X
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float xe = x[e] + xl[e];
-          v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
+          for (int e = 0; e < 32; ++e)
+            v[e] = fmaf(p.ca, x[e] + xl[e], __uint_as_float(r[e])) * ms;
+        } else {
+          // P = bS + cS^2 + (a - 1) I; its diagonal's rounding residual d
+          const float d = p.pdiag_in[static_cast<int64_t>(b) * p.pdiag_bstride + row];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float xe = x[e] + xl[e];
+            v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
+          }
         }
       }
     }
-    if ((EPI == kEpiGram || EPI == kEpiPoly) && p.pdiag != nullptr && row >= col0 &&
+    if ((K == kEpiGram || K == kEpiPoly) && (p.pdiag != nullptr || kX3) && row >= col0 &&
         row < col0 + 32) {
       // the (a - 1) I shift; the diagonal's bf16 rounding residual is kept
       // in fp32 so that P's diagonal is exact to fp32 in the update
@@ -428,8 +460,9 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
       for (int e = 0; e < 32; ++e)
         if (col0 + e == row) {
           v[e] += p.cd;
-          p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
-              v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+          if (p.pdiag != nullptr)
+            p.pdiag[static_cast<int64_t>(b) * p.pdiag_bstride + row] =
+                v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
         }
     }
     if (kFin) {
@@ -465,10 +498,15 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
       // transposed copy: for each column e the warp's 32 lanes (32
       // consecutive rows) store 64 contiguous bytes of row col0 + e
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = __float2bfloat16_rn(v[e]);
+      for (int e = 0; e < 32; ++e) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v[e]);
+        out[static_cast<int64_t>(col0 + e) * p.out_ld + row] = h;
+        if (kX3 && lo_out)
+          out[static_cast<int64_t>(col0 + e) * p.out_ld + row + p.lo_off] =
+              __float2bfloat16_rn(v[e] - __bfloat162float(h));
+      }
     }
-    if (EPI != kEpiGram) {
+    if (K != kEpiGram) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         cur_h[k] = nxt_h[k];
@@ -487,8 +525,9 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
 // arrives on the stage's empty barrier in both CTAs).
 template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+    k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+              const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+              const GemmParams p) {
   static_assert(!(SYM && PAIR) || BN == 256, "symmetric pairs are 256-row super-rows");
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
@@ -527,7 +566,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (p.kplanes > 1) tma_prefetch_desc(&tmB2);
+    if (p.b_lo_mask) tma_prefetch_desc(&tmB2);
+    if (p.a_lo_mask) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -552,16 +592,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         int b, tm, tn;
         decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
+        int plane = 0, kk = 0;                     // operand plane, k-block within it
         for (int kb = 0; kb < nkb_total; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
-          const bool second = kb >= nkb;           // second plane of the B operand
-          const int k0 = (second ? kb - nkb : kb) * kBK;
-          const CUtensorMap* tb = second ? &tmB2 : &tmB;
+          const int k0 = kk * kBK;
+          const CUtensorMap* ta = ((p.a_lo_mask >> plane) & 1) ? &tmA2 : &tmA;
+          const CUtensorMap* tb = ((p.b_lo_mask >> plane) & 1) ? &tmB2 : &tmB;
+          if (++kk == nkb) {
+            kk = 0;
+            ++plane;
+          }
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          tma_load_3d(smA + stage * C::kABytes, &tmA, &full[stage], k0, tm * kBM, b);
+          tma_load_3d(smA + stage * C::kABytes, ta, &full[stage], k0, tm * kBM, b);
           if (PAIR) {
             // this CTA's half of B, into both CTAs (the B map's box is half the tile)
             if (!B_MN) {
@@ -702,8 +747,9 @@ constexpr size_t kSmemBytes2 = kStages2 * kStageBytes2 + 1024 + 256;
 
 template <bool B_MN, int EPI, bool SYM>
 __global__ void __launch_bounds__(kGemmThreads2, 1)
-    k_ns_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+    k_ns_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+               const GemmParams p) {
   constexpr int BN = 256;
   constexpr uint32_t kTmemCols = kAccBufs2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, B_MN);
@@ -742,7 +788,8 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
     fence_proxy_async_smem();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (p.kplanes > 1) tma_prefetch_desc(&tmB2);
+    if (p.b_lo_mask) tma_prefetch_desc(&tmB2);
+    if (p.a_lo_mask) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -768,17 +815,22 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
       for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         int b, tm, tn;
         decode_unit<BN, SYM, true>(p, t, rank, b, tm, tn);
+        int plane = 0, kk = 0;
         for (int kb = 0; kb < nkb_total; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
-          const bool second = kb >= nkb;
-          const int k0 = (second ? kb - nkb : kb) * kBK;
-          const CUtensorMap* tb = second ? &tmB2 : &tmB;
+          const int k0 = kk * kBK;
+          const CUtensorMap* ta = ((p.a_lo_mask >> plane) & 1) ? &tmA2 : &tmA;
+          const CUtensorMap* tb = ((p.b_lo_mask >> plane) & 1) ? &tmB2 : &tmB;
+          if (++kk == nkb) {
+            kk = 0;
+            ++plane;
+          }
           const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes2);
-          tma_load_3d_pair(smA + stage * kHalfBytes2, &tmA, bar, k0, tm * kBM, b);
+          tma_load_3d_pair(smA + stage * kHalfBytes2, ta, bar, k0, tm * kBM, b);
           if (!B_MN) {
             tma_load_3d_pair(smB + stage * kHalfBytes2, tb, bar, k0,
                              tn * BN + static_cast<int>(rank) * 128, b);
@@ -935,14 +987,16 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int batch, int K, int N) {
 }
 
 template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
-cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                        const GemmParams& p, double alg_flops, cudaStream_t st) {
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+                        const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
+                        cudaStream_t st) {
   auto kern = k_ns_gemm<BN, B_MN, EPI, SYM, PAIR>;
   const size_t smem = Cfg<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
+  const KernelKind kind = epi_kind(EPI) == kEpiGram ? kKindGram
+                          : (epi_kind(EPI) == kEpiPoly ? kKindPoly : kKindUpdate);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kGemmThreads);
@@ -971,7 +1025,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     cfg.numAttrs += 1;
   }
   prof_begin(kind, st);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -979,13 +1033,15 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
 
 
 template <bool B_MN, int EPI, bool SYM>
-cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb2,
-                         const GemmParams& p, double alg_flops, cudaStream_t st) {
+cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
+                         const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
+                         cudaStream_t st) {
   auto kern = k_ns_gemm2<B_MN, EPI, SYM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kSmemBytes2));
   if (e != cudaSuccess) return e;
-  const KernelKind kind = EPI == kEpiGram ? kKindGram : (EPI == kEpiPoly ? kKindPoly : kKindUpdate);
+  const KernelKind kind = epi_kind(EPI) == kEpiGram ? kKindGram
+                          : (epi_kind(EPI) == kEpiPoly ? kKindPoly : kKindUpdate);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1010,22 +1066,66 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
     cfg.numAttrs = 2;
   }
   prof_begin(kind, st);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, p);
   prof_end(kind, st, alg_flops, 0.0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 
+// Tensor maps of one operand: K-major with 128-row boxes (A, and the B half a
+// CTA of a pair loads) and BN-row boxes (unpaired B), MN-major (the update's
+// B), each for the hi and the lo plane.  Operands without a lo plane carry
+// their hi map in the lo slots (never read: the plane masks select hi only).
 struct OperandMaps {
-  CUtensorMap k128, kbn, mn, mn_lo;
+  CUtensorMap k128, kbn, mn, k128_lo, kbn_lo, mn_lo;
 };
+
+// Gram / polynomial: A and B are the same symmetric operand (X or S).
+template <int EPI>
+cudaError_t launch_sym(int bn, bool pair, const OperandMaps& A, const GemmParams& p, double f,
+                       cudaStream_t st) {
+  if (bn == 256 && pair && kUseTwoSm)
+    return launch_gemm2<false, EPI, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, p, f, st);
+  if (bn == 256 && pair)
+    return launch_gemm<256, false, EPI, true, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, p, f, st);
+  if (bn == 256)
+    return launch_gemm<256, false, EPI, true, false>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
+  return launch_gemm<128, false, EPI, true, false>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
+}
+
+// Update: A = P (K-major), B = X (MN-major).
+template <int EPI>
+cudaError_t launch_upd(int bn, bool pair, const OperandMaps& Pm, const OperandMaps& Xm,
+                       const GemmParams& p, double f, cudaStream_t st) {
+  if (bn == 256 && pair && kUseTwoSm)
+    return launch_gemm2<true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+  if (bn == 256 && pair)
+    return launch_gemm<256, true, EPI, false, true>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+  if (bn == 256)
+    return launch_gemm<256, true, EPI, false, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+  if (pair)
+    return launch_gemm<128, true, EPI, false, true>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+  return launch_gemm<128, true, EPI, false, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+}
+
+bool map_square(OperandMaps* o, const __nv_bfloat16* hi, const __nv_bfloat16* lo, int batch, int n,
+                int bn) {
+  if (!map_kmajor(&o->k128, hi, batch, n, n, kBM) || !map_kmajor(&o->kbn, hi, batch, n, n, bn))
+    return false;
+  if (lo == nullptr) {
+    o->k128_lo = o->k128;
+    o->kbn_lo = o->kbn;
+    return true;
+  }
+  return map_kmajor(&o->k128_lo, lo, batch, n, n, kBM) && map_kmajor(&o->kbn_lo, lo, batch, n, n, bn);
+}
 
 }  // namespace
 
-bool ns_final_fused(int iters) { return iters > kLoIters; }
+bool ns_final_fused(int iters, bool x3) { return !x3 && iters > kLoIters; }
 
-bool ns_final_has_lo(int iters) { return iters < kLoIters; }
+bool ns_final_has_lo(int iters, bool x3) { return x3 || iters < kLoIters; }
 
 cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   if (a.iters == 0) return cudaSuccess;
@@ -1033,28 +1133,35 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   const int n = a.n_pad, m = a.m_pad, batch = a.batch;
   const int bn_sq = (n % 256 == 0) ? 256 : 128;
   const int bn_up = (m % 256 == 0) ? 256 : 128;
+  const bool x3 = a.x3 != 0;
 
   OperandMaps X[2], S, P;
   __nv_bfloat16* xb[2] = {a.X0, a.X1};
   for (int i = 0; i < 2; ++i) {
+    const __nv_bfloat16* lo = xb[i] + a.lo_off;
     if (!map_kmajor(&X[i].k128, xb[i], batch, n, m, kBM) ||
         !map_kmajor(&X[i].kbn, xb[i], batch, n, m, bn_sq) ||
         !map_mnmajor(&X[i].mn, xb[i], batch, n, m) ||
-        !map_mnmajor(&X[i].mn_lo, xb[i] + a.lo_off, batch, n, m))
+        !map_kmajor(&X[i].k128_lo, lo, batch, n, m, kBM) ||
+        !map_kmajor(&X[i].kbn_lo, lo, batch, n, m, bn_sq) ||
+        !map_mnmajor(&X[i].mn_lo, lo, batch, n, m))
       return cudaErrorInvalidValue;
   }
-  if (!map_kmajor(&S.k128, a.A, batch, n, n, kBM) || !map_kmajor(&S.kbn, a.A, batch, n, n, bn_sq) ||
-      !map_kmajor(&P.k128, a.B, batch, n, n, kBM) || !map_kmajor(&P.kbn, a.B, batch, n, n, bn_sq))
+  if (!map_square(&S, a.A, x3 ? a.A + a.sq_lo_off : nullptr, batch, n, bn_sq) ||
+      !map_square(&P, a.B, x3 ? a.B + a.sq_lo_off : nullptr, batch, n, bn_sq))
     return cudaErrorInvalidValue;
 
   // Algorithmic flops per launch (unpadded n x m, symmetric products at half
   // their dense count): Gram n^2 m, polynomial n^3, update 2 n^2 m per matrix.
+  // The split-bf16 precision does three products for each (not counted).
   const double nr = a.n, mr = a.m;
   const double f_gram = batch * nr * nr * mr, f_poly = batch * nr * nr * nr,
                f_update = 2.0 * batch * nr * nr * mr;
   const int tm_sq = n / kBM;
   const int S_sq = n / bn_sq;
   const int sym_tiles = (bn_sq / kBM) * S_sq * (S_sq + 1) / 2;
+  // split-bf16: planes (hi, hi), (hi, lo), (lo, hi) of (A, B)
+  const int x3_planes = 3, x3_a_lo = 0b100, x3_b_lo = 0b010;
 
   for (int it = 0; it < a.iters; ++it) {
     const float ca = a.coeffs[3 * it], cb = a.coeffs[3 * it + 1], cc = a.coeffs[3 * it + 2];
@@ -1073,20 +1180,18 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.out = (cc != 0.f) ? a.A : a.B;   // c == 0: the Gram epilogue writes P directly
     g.out_ld = n; g.out_bstride = static_cast<int64_t>(n) * n;
     g.cb = (cc != 0.f) ? 1.f : cb;
-    g.cd = (cc != 0.f) ? 0.f : ca - 1.f;
-    g.pdiag = (cc != 0.f) ? nullptr : a.pdiag;
+    g.cd = (cc != 0.f || x3) ? 0.f : ca - 1.f;   // split-bf16: no (a - 1) I shift
+    g.pdiag = (cc != 0.f || x3) ? nullptr : a.pdiag;
     g.pdiag_bstride = n;
     g.kplanes = 1;
+    if (x3) {
+      g.kplanes = x3_planes; g.a_lo_mask = x3_a_lo; g.b_lo_mask = x3_b_lo;
+      g.lo_off = a.sq_lo_off; g.lo_out = 1;
+    }
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    if (bn_sq == 256 && pair && kUseTwoSm)
-      e = launch_gemm2<false, kEpiGram, true>(X[cur].k128, X[cur].k128, X[cur].k128, g, f_gram, st);
-    else if (bn_sq == 256 && pair)
-      e = launch_gemm<256, false, kEpiGram, true, true>(X[cur].k128, X[cur].k128, X[cur].k128, g, f_gram, st);
-    else if (bn_sq == 256)
-      e = launch_gemm<256, false, kEpiGram, true, false>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
-    else
-      e = launch_gemm<128, false, kEpiGram, true, false>(X[cur].k128, X[cur].kbn, X[cur].kbn, g, f_gram, st);
+    e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], g, f_gram, st)
+           : launch_sym<kEpiGram>(bn_sq, pair, X[cur], g, f_gram, st);
     if (e != cudaSuccess) return e;
 
     if (cc != 0.f) {
@@ -1094,17 +1199,12 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.K = n;
       q.out = a.B;
       q.aux = a.A; q.aux_ld = n; q.aux_bstride = static_cast<int64_t>(n) * n;
-      q.cb = cb; q.cc = cc; q.cd = ca - 1.f;
-      q.pdiag = a.pdiag;
+      q.cb = cb; q.cc = cc; q.cd = x3 ? 0.f : ca - 1.f;
+      q.pdiag = x3 ? nullptr : a.pdiag;
       q.mscale = nullptr;
-      if (bn_sq == 256 && pair && kUseTwoSm)
-        e = launch_gemm2<false, kEpiPoly, true>(S.k128, S.k128, S.k128, q, f_poly, st);
-      else if (bn_sq == 256 && pair)
-        e = launch_gemm<256, false, kEpiPoly, true, true>(S.k128, S.k128, S.k128, q, f_poly, st);
-      else if (bn_sq == 256)
-        e = launch_gemm<256, false, kEpiPoly, true, false>(S.k128, S.kbn, S.kbn, q, f_poly, st);
-      else
-        e = launch_gemm<128, false, kEpiPoly, true, false>(S.k128, S.kbn, S.kbn, q, f_poly, st);
+      if (x3) q.lo_in = 1;
+      e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, q, f_poly, st)
+             : launch_sym<kEpiPoly>(bn_sq, pair, S, q, f_poly, st);
       if (e != cudaSuccess) return e;
     }
 
@@ -1118,40 +1218,29 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.lo_off = a.lo_off;
     u.ca = 1.f; u.cb = 1.f; u.cc = 0.f; u.cd = 0.f;
     u.pdiag_in = a.pdiag; u.pdiag_bstride = n;
-    u.kplanes = (it < kResidualIters) ? 2 : 1;
-    u.lo_in = it < kLoIters;
-    u.lo_out = it + 1 < kLoIters;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
-    const bool fin = (it + 1 == a.iters) && a.fin.mode != 0;
-    if (fin) {
+    if (x3) {
+      u.kplanes = x3_planes; u.a_lo_mask = x3_a_lo; u.b_lo_mask = x3_b_lo;
+      u.lo_in = 1; u.lo_out = 1;
+      u.ca = ca;
+      e = launch_upd<kEpiUpdate | kEpiX3>(bn_up, pair, P, X[cur], u, f_update, st);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
+    u.kplanes = (it < kResidualIters) ? 2 : 1;   // product reads X hi (and lo)
+    u.b_lo_mask = (u.kplanes == 2) ? 0b10 : 0;
+    u.lo_in = it < kLoIters;
+    u.lo_out = it + 1 < kLoIters;
+    if ((it + 1 == a.iters) && a.fin.mode != 0) {
       // the last update writes W (or the output); it has no lo plane
       u.fin = a.fin;
       u.lo_in = false;
       u.lo_out = false;
-      if (bn_up == 256 && pair && kUseTwoSm)
-        e = launch_gemm2<true, kEpiFinal, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-      else if (bn_up == 256 && pair)
-        e = launch_gemm<256, true, kEpiFinal, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-      else if (bn_up == 256)
-        e = launch_gemm<256, true, kEpiFinal, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-      else if (pair)
-        e = launch_gemm<128, true, kEpiFinal, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-      else
-        e = launch_gemm<128, true, kEpiFinal, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-      if (e != cudaSuccess) return e;
-      continue;
+      e = launch_upd<kEpiFinal>(bn_up, pair, P, X[cur], u, f_update, st);
+    } else {
+      e = launch_upd<kEpiUpdate>(bn_up, pair, P, X[cur], u, f_update, st);
     }
-    if (bn_up == 256 && pair && kUseTwoSm)
-      e = launch_gemm2<true, kEpiUpdate, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-    else if (bn_up == 256 && pair)
-      e = launch_gemm<256, true, kEpiUpdate, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-    else if (bn_up == 256)
-      e = launch_gemm<256, true, kEpiUpdate, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-    else if (pair)
-      e = launch_gemm<128, true, kEpiUpdate, false, true>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
-    else
-      e = launch_gemm<128, true, kEpiUpdate, false, false>(P.k128, X[cur].mn, X[cur].mn_lo, u, f_update, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -170,10 +170,14 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
+// Arrive on an mbarrier of another CTA of the cluster, with the default
+// (release, CTA-scope) semantics.  Used to hand a TMEM accumulator back to
+// the MMA issuer: the data dependence is carried by tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync, and the waiter reads nothing this
+// thread stored, so a cluster-scope release (which waits for every earlier
+// global store of the thread to be acknowledged) is not needed.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -153,9 +153,19 @@ def test_view_validation(lib, rows, cols, rs, want):
     assert code == want
 
 
+def test_split_bf16_workspace_adds_lo_planes_of_s_and_p(lib):
+    x3 = m.Schedule([(1, (1.0, 0.0, 0.0))], prec=m.MUON_NS_BF16X3)
+    code, nb = _ws_size([_group(1024, 1024, batch=64)])
+    code3, nb3 = _ws_size([_group(1024, 1024, batch=64)], x3.ref)
+    assert code == code3 == m.MUON_OK
+    assert nb3 == nb + 2 * 64 * 1024 * 1024 * 2
+
+
 def test_schedule_validation(lib):
     tf32 = m.Schedule([(1, (1.0, 0.0, 0.0))], prec=m.MUON_NS_TF32)
     assert _ws_size([_group(8, 8)], tf32.ref)[0] == m.MUON_ERR_UNSUPPORTED
+    other = m.Schedule([(1, (1.0, 0.0, 0.0))], prec=7)
+    assert _ws_size([_group(8, 8)], other.ref)[0] == m.MUON_ERR_INVALID_ARG
     bad = m.Schedule([(-1, (1.0, 0.0, 0.0))])
     assert _ws_size([_group(8, 8)], bad.ref)[0] == m.MUON_ERR_INVALID_ARG
     nan = m.Schedule([(1, (float("nan"), 0.0, 0.0))])
