@@ -287,23 +287,23 @@ def run_reference(args):
     return 0
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=("ns_gemm.cu", "ptx.cuh")):
     h = hashlib.sha256()
-    for f in ("ns_gemm.cu", "ptx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "newton_schulz_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel: str):
+def read_traffic(kernel: str, summary="ns_gemm_traffic.json", files=("ns_gemm.cu", "ptx.cuh")):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    p = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
+    if d.get("source_hash") != kernel_source_hash(files):
         return None
     e = d.get("kernels", {}).get(kernel)
     if not e:
@@ -623,7 +623,8 @@ def run_adamw(args):
     per_launch = d["alg_bytes"] / d["launches"]
     achieved = per_launch / avg_s / 1e9
     roof = {"kernel": "adamw", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "traffic": read_traffic("adamw", "adamw_traffic.json", ("adamw.cu",)),
             "alg_bytes_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
             "timing": f"event pair per launch, {prof_steps} profiled steps after the timed region",
             "peak_source": f"{peak_src} copy"}
