@@ -129,7 +129,6 @@ struct GemmParams {
   uint32_t* status;
   uint64_t timeout_ns;
   FinalStore fin;   // update, last iteration: fused scale / decay / store
-  int reverse;      // walk the tiles from the last matrix back to the first
 };
 
 // Tile t -> (matrix, tile row, tile column).  For symmetric outputs only the
@@ -163,7 +162,6 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& b, 
 template <int BN, bool SYM, bool PAIR>
 __device__ __forceinline__ void decode_unit(const GemmParams& p, int t, uint32_t rank, int& b,
                                             int& tm, int& tn) {
-  if (p.reverse) t = p.total_tiles - 1 - t;
   if (!PAIR) {
     decode_tile<BN, SYM>(p, t, b, tm, tn);
     return;
@@ -1172,9 +1170,6 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   // split-bf16: planes (hi, hi), (hi, lo), (lo, hi) of (A, B)
   const int x3_planes = 3, x3_a_lo = 0b100, x3_b_lo = 0b010;
 
-  // Consecutive GEMMs walk the batch in opposite directions: each starts on
-  // the matrices its predecessor wrote last, whose outputs are still in L2.
-  int dir = 1;   // the prepare pass wrote the iterate in matrix order
   for (int it = 0; it < a.iters; ++it) {
     const float ca = a.coeffs[3 * it], cb = a.coeffs[3 * it + 1], cc = a.coeffs[3 * it + 2];
     const int cur = it & 1;
@@ -1202,7 +1197,6 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     }
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    g.reverse = dir; dir ^= 1;
     e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], g, f_gram, st)
            : launch_sym<kEpiGram>(bn_sq, pair, X[cur], g, f_gram, st);
     if (e != cudaSuccess) return e;
@@ -1215,7 +1209,6 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.cb = cb; q.cc = cc; q.cd = x3 ? 0.f : ca - 1.f;
       q.pdiag = x3 ? nullptr : a.pdiag;
       q.mscale = nullptr;
-      q.reverse = dir; dir ^= 1;
       if (x3) q.lo_in = 1;
       e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, q, f_poly, st)
              : launch_sym<kEpiPoly>(bn_sq, pair, S, q, f_poly, st);
@@ -1234,7 +1227,6 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.pdiag_in = a.pdiag; u.pdiag_bstride = n;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
-    u.reverse = dir; dir ^= 1;
     if (x3) {
       u.kplanes = x3_planes; u.a_lo_mask = x3_a_lo; u.b_lo_mask = x3_b_lo;
       u.lo_in = 1; u.lo_out = 1;
