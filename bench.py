@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--prof-steps", type=int, default=50)
+    ap.add_argument("--merge", type=int, choices=[0, 1], default=0,
+                    help="dense / moe: groups of one wide shape share a Newton–Schulz chain")
     ap.add_argument("--prec", choices=["bf16", "x3"], default="bf16",
                     help="Newton–Schulz precision: bf16 (default) or split-bf16 (MUON_NS_BF16X3)")
     return ap.parse_args()
@@ -339,9 +341,12 @@ def run_ours(args):
         P = n_params(wl)
     hp = m.hparams()
     sched = None
-    if args.prec == "x3":
+    merge = args.merge == 1 and args.workload in ("dense", "moe")
+    if args.prec == "x3" or merge:
         sched = m.muon_ns_hybrid_schedule()
-        sched.prec = m.MUON_NS_BF16X3
+        if args.prec == "x3":
+            sched.prec = m.MUON_NS_BF16X3
+        sched.merge_groups = 1 if merge else 0
     ws = m.workspace(m.muon_step_workspace_size(groups[0], sched), device=dev)
     stream = torch.cuda.current_stream()
 
@@ -476,6 +481,8 @@ def run_ours(args):
     desc = dict(wl["desc"])
     desc["ns_precision"] = {"bf16": "bf16 (MUON_NS_BF16)",
                             "x3": "split-bf16 (MUON_NS_BF16X3, three products per GEMM)"}[args.prec]
+    if wl["kind"] in ("dense", "moe"):
+        desc["merge_groups"] = bool(merge)
     desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
                 l2={"stack": "inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M "
                              "+ 768 MiB workspace",

@@ -107,12 +107,20 @@ typedef struct {
 
 /* stages: host array of n_stages entries (read during the call only).
  * normalize: 1 = divide by the Frobenius norm first (the page's behaviour),
- *            0 = iterate the input as is. */
+ *            0 = iterate the input as is.
+ * merge_groups (muon_step_batched / muon_step_workspace_size only):
+ *            1 = groups whose matrices have the same wide shape (min and max
+ *            of rows, cols), in either orientation, share one Newton–Schulz
+ *            chain of up to 4 groups (a 14336 x 4096 weight group and a
+ *            4096 x 14336 one run as one batch: fewer launches, fuller
+ *            waves; results are bit-identical to unmerged, the workspace is
+ *            sized for the merged batches); 0 = one chain per group. */
 typedef struct {
   const muon_ns_stage_t* stages;
   int n_stages;
   int normalize;
   muon_ns_precision_t prec;
+  int merge_groups;
 } muon_ns_schedule_t;
 
 /* A matrix view in elements.  rows x cols, row-major, unit column stride.

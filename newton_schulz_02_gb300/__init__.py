@@ -47,7 +47,7 @@ class muon_ns_stage_t(ctypes.Structure):
 
 class muon_ns_schedule_t(ctypes.Structure):
     _fields_ = [("stages", POINTER(muon_ns_stage_t)), ("n_stages", c_int), ("normalize", c_int),
-                ("prec", c_int)]
+                ("prec", c_int), ("merge_groups", c_int)]
 
 
 class muon_view_t(ctypes.Structure):
@@ -165,13 +165,14 @@ def _stream(stream) -> Optional[int]:
 class Schedule:
     """Owns a muon_ns_schedule_t and its stage array."""
 
-    def __init__(self, stages: Sequence, normalize: bool = True, prec: int = MUON_NS_BF16):
+    def __init__(self, stages: Sequence, normalize: bool = True, prec: int = MUON_NS_BF16,
+                 merge_groups: bool = False):
         arr = (muon_ns_stage_t * max(1, len(stages)))()
         for i, (steps, (a, b, c)) in enumerate(stages):
             arr[i] = muon_ns_stage_t(int(steps), float(a), float(b), float(c))
         self._arr = arr
         self.c = muon_ns_schedule_t(ctypes.cast(arr, POINTER(muon_ns_stage_t)), len(stages),
-                                    int(bool(normalize)), int(prec))
+                                    int(bool(normalize)), int(prec), int(bool(merge_groups)))
 
     @property
     def ref(self):

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) k_prepare_wide(PrepareArgs p) {
     *reinterpret_cast<uint4*>(X + p.x_lo_off + o) = lo;
   }
   const float s = block_sum(acc, red);
-  if (threadIdx.x == 0) p.partials[static_cast<int64_t>(b) * p.parts + blockIdx.x] = s;
+  if (threadIdx.x == 0) p.partials[static_cast<int64_t>(b) * p.parts_stride + blockIdx.x] = s;
 }
 
 // ---- pass 1, tall (rows > cols): X_ws[j][i] = X[i][j] via 64x64 smem tiles ---
@@ -240,15 +240,19 @@ __global__ void __launch_bounds__(kThreads) k_prepare_tall(PrepareArgs p) {
     __syncthreads();
   }
   const float s = block_sum(acc, red);
-  if (threadIdx.x == 0) p.partials[static_cast<int64_t>(b) * p.parts + blockIdx.x] = s;
+  if (threadIdx.x == 0) p.partials[static_cast<int64_t>(b) * p.parts_stride + blockIdx.x] = s;
 }
 
 // ---- per-matrix norm ------------------------------------------------------------
 __global__ void k_finalize_norm(FinalizeArgs p) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.batch) return;
+  int seg = 0;
+  while (seg + 1 < p.nseg && b >= p.seg_begin[seg + 1]) ++seg;
+  const int parts = p.seg_parts[seg];
   double s = 0.0;
-  for (int k = 0; k < p.parts; ++k) s += static_cast<double>(p.partials[static_cast<int64_t>(b) * p.parts + k]);
+  for (int k = 0; k < parts; ++k)
+    s += static_cast<double>(p.partials[static_cast<int64_t>(b) * p.parts_stride + k]);
   if (!isfinite(s)) atomicOr(p.status, kFlagNonFinite);
   float inv;
   if (p.skip[b]) {
@@ -406,7 +410,7 @@ cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st) {
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st) {
   prof_begin(kKindFinalize, st);
   k_finalize_norm<<<(a.batch + 127) / 128, 128, 0, st>>>(a);
-  prof_end(kKindFinalize, st, 0.0, static_cast<double>(a.batch) * (a.parts * 4.0 + 4.0));
+  prof_end(kKindFinalize, st, 0.0, static_cast<double>(a.batch) * (a.parts_stride * 4.0 + 4.0));
   return cudaGetLastError();
 }
 

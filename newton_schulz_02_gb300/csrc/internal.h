@@ -52,14 +52,23 @@ struct PrepareArgs {
   int n_pad, m_pad;
   int tall;             // rows > cols: X holds the transpose
   int parts;            // blocks per matrix (partials per matrix)
-  float* partials;      // [batch][parts]
+  int parts_stride;     // partials between consecutive matrices (>= parts)
+  float* partials;      // [batch][parts_stride]
   uint8_t* skip;        // [batch], set to 1 for a matrix with a misaligned pointer
   uint32_t* status;
 };
 
+// Groups of matrices that share one Newton–Schulz chain (same wide shape,
+// either orientation) go through it as one batch of at most kMaxMerge
+// segments.
+constexpr int kMaxMerge = 4;
+
 struct FinalizeArgs {
-  int batch, parts;
-  const float* partials;
+  int batch, parts_stride;
+  int nseg;
+  int seg_begin[kMaxMerge];   // first matrix of each segment
+  int seg_parts[kMaxMerge];   // partials per matrix in each segment
+  const float* partials;      // [batch][parts_stride]
   const uint8_t* skip;
   float* inv_s;  // [batch]: 1/||X||_F (0 for a zero or skipped matrix); 1 if !normalize
   int normalize;
@@ -89,19 +98,26 @@ struct ApplyArgs {
 // Last-iteration store fused into the update epilogue: mode 1 applies
 // W <- W*(1 - lr*wd*mask) - lr*scale*O' (muon_step_batched), mode 2 writes O'
 // into a dense output (newton_schulz_batched); mode 0 keeps the iterate in the
-// workspace for a separate last pass.
-struct FinalStore {
-  int mode;
+// workspace for a separate last pass.  One segment per group of the chain's
+// batch (matrices seg[s].begin .. seg[s+1].begin - 1).
+struct FinalSeg {
+  int begin;                 // first matrix of the segment in the chain's batch
   int rows, cols;            // W / output shape in its own orientation
   int tall;                  // rows > cols: the wide element (i, j) is W[j][i]
   int dtype;                 // W dtype (mode 1) or output dtype (mode 2)
-  void* const* w_ptrs;       // mode 1: device array of W pointers
+  void* const* w_ptrs;       // mode 1: device array of W pointers (segment-local index)
   int64_t w_ld;              // mode 1: W row stride (elements)
-  void* out_base;            // mode 2: dense [batch][rows][cols]
-  const uint8_t* wd_mask;    // mode 1: decay mask, or nullptr (all on)
-  const uint8_t* skip;       // matrices to leave untouched
+  void* out_base;            // mode 2: dense [segment batch][rows][cols]
+  const uint8_t* wd_mask;    // mode 1: decay mask (segment-local), or nullptr (all on)
   float decay_on;            // 1 - lr*wd
   float lr_scale;            // lr * scale
+};
+
+struct FinalStore {
+  int mode;
+  int nseg;
+  const uint8_t* skip;       // [chain batch]: matrices to leave untouched
+  FinalSeg seg[kMaxMerge];
 };
 
 struct NsChainArgs {

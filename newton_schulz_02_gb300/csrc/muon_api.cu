@@ -48,12 +48,17 @@ struct Layout {
   size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
 };
 
-Layout layout_for(int batch, int rows, int cols, bool x3) {
+int wide_n(const muon_view_t& v) { return v.rows < v.cols ? v.rows : v.cols; }
+int wide_m(const muon_view_t& v) { return v.rows < v.cols ? v.cols : v.rows; }
+
+// Workspace of one Newton–Schulz chain over `batch` matrices of padded wide
+// shape n_pad x m_pad whose prepare passes write up to `parts` partial sums
+// per matrix.
+Layout layout_for(int batch, int n_pad, int m_pad, int parts, bool x3) {
   Layout L;
-  const int n = rows < cols ? rows : cols, m = rows < cols ? cols : rows;
-  L.n_pad = static_cast<int>(round_up(n, kPad));
-  L.m_pad = static_cast<int>(round_up(m, kPad));
-  L.parts = prepare_parts(rows, cols, L.n_pad, L.m_pad);
+  L.n_pad = n_pad;
+  L.m_pad = m_pad;
+  L.parts = parts;
   const size_t xb = static_cast<size_t>(batch) * L.n_pad * L.m_pad * 2;
   const size_t sb = static_cast<size_t>(batch) * L.n_pad * L.n_pad * 2;
   L.lo_off = static_cast<int64_t>(align256(xb) / 2);
@@ -73,6 +78,50 @@ Layout layout_for(int batch, int rows, int cols, bool x3) {
   return L;
 }
 
+Layout layout_for(int batch, const muon_view_t& v, bool x3) {
+  const int n_pad = static_cast<int>(round_up(wide_n(v), kPad));
+  const int m_pad = static_cast<int>(round_up(wide_m(v), kPad));
+  return layout_for(batch, n_pad, m_pad, prepare_parts(v.rows, v.cols, n_pad, m_pad), x3);
+}
+
+// Groups of one muon_step_batched call, cut into Newton–Schulz chains.  With
+// merging, groups of the same wide shape (n, m) -- either orientation, so a
+// 14336 x 4096 weight and a 4096 x 14336 one share a chain -- go through one
+// chain of at most kMaxMerge groups, in order of first appearance;
+// otherwise every group has its own chain.
+struct Chain {
+  std::vector<int> members;  // group indices, in batch order
+  int batch = 0, n = 0, m = 0, n_pad = 0, m_pad = 0, parts = 0;
+};
+
+std::vector<Chain> plan_chains(const muon_group_t* groups, int n_groups, bool merge) {
+  std::vector<Chain> chains;
+  for (int i = 0; i < n_groups; ++i) {
+    const muon_view_t& v = groups[i].view;
+    const int n = wide_n(v), m = wide_m(v);
+    Chain* c = nullptr;
+    if (merge)
+      for (Chain& k : chains)
+        if (k.n == n && k.m == m && static_cast<int>(k.members.size()) < kMaxMerge) {
+          c = &k;
+          break;
+        }
+    if (c == nullptr) {
+      chains.emplace_back();
+      c = &chains.back();
+      c->n = n;
+      c->m = m;
+      c->n_pad = static_cast<int>(round_up(n, kPad));
+      c->m_pad = static_cast<int>(round_up(m, kPad));
+    }
+    c->members.push_back(i);
+    c->batch += groups[i].batch;
+    const int parts = prepare_parts(v.rows, v.cols, c->n_pad, c->m_pad);
+    if (parts > c->parts) c->parts = parts;
+  }
+  return chains;
+}
+
 muon_status_t check_view(const muon_view_t& v) {
   if (v.rows < 1 || v.cols < 1 || v.rows > kMaxDim || v.cols > kMaxDim) return MUON_ERR_INVALID_ARG;
   if (v.row_stride < v.cols) return MUON_ERR_INVALID_ARG;
@@ -83,7 +132,7 @@ muon_status_t check_view(const muon_view_t& v) {
 }
 
 muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* coeffs,
-                              int* normalize, bool* x3) {
+                              int* normalize, bool* x3, bool* merge = nullptr) {
   muon_ns_schedule_t def;
   if (s == nullptr) {
     muon_ns_hybrid_schedule(&def);
@@ -93,6 +142,7 @@ muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* c
   if (s->prec != MUON_NS_BF16 && s->prec != MUON_NS_BF16X3) return MUON_ERR_INVALID_ARG;
   if (s->n_stages < 0 || (s->n_stages > 0 && s->stages == nullptr)) return MUON_ERR_INVALID_ARG;
   if (s->normalize != 0 && s->normalize != 1) return MUON_ERR_INVALID_ARG;
+  if (s->merge_groups != 0 && s->merge_groups != 1) return MUON_ERR_INVALID_ARG;
   coeffs->clear();
   for (int i = 0; i < s->n_stages; ++i) {
     const muon_ns_stage_t& st = s->stages[i];
@@ -107,6 +157,7 @@ muon_status_t expand_schedule(const muon_ns_schedule_t* s, std::vector<float>* c
   }
   *normalize = s->normalize;
   *x3 = (s->prec == MUON_NS_BF16X3);
+  if (merge != nullptr) *merge = (s->merge_groups == 1);
   return MUON_OK;
 }
 
@@ -127,14 +178,28 @@ double update_scale(const muon_view_t& v, muon_scale_mode_t mode, float gamma) {
 
 muon_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MUON_OK : MUON_ERR_CUDA; }
 
-// Shared tail of both entry points: norm, NS chain, last pass.
-muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_view_t& v,
-                             const std::vector<float>& coeffs, int normalize, bool x3,
-                             ApplyArgs ap, cudaStream_t st) {
+// One segment of a chain: a group's matrices [begin, begin + batch) and the
+// arguments of its last pass (W update or dense output).
+struct Segment {
+  int begin = 0, batch = 0, parts = 0;
+  muon_view_t view{};
+  ApplyArgs ap{};
+};
+
+// Shared tail of both entry points: norm, NS chain, last pass, over the
+// chain's segments (each already prepared into its slice of the workspace).
+muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
+                             const std::vector<Segment>& segs, const std::vector<float>& coeffs,
+                             int normalize, bool x3, cudaStream_t st) {
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   FinalizeArgs fa{};
   fa.batch = batch;
-  fa.parts = L.parts;
+  fa.parts_stride = L.parts;
+  fa.nseg = static_cast<int>(segs.size());
+  for (size_t k = 0; k < segs.size(); ++k) {
+    fa.seg_begin[k] = segs[k].begin;
+    fa.seg_parts[k] = segs[k].parts;
+  }
   fa.partials = reinterpret_cast<const float*>(ws + L.partials);
   fa.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
   fa.inv_s = reinterpret_cast<float*>(ws + L.inv_s);
@@ -148,8 +213,8 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   na.batch = batch;
   na.n_pad = L.n_pad;
   na.m_pad = L.m_pad;
-  na.n = v.rows < v.cols ? v.rows : v.cols;
-  na.m = v.rows < v.cols ? v.cols : v.rows;
+  na.n = n;
+  na.m = m;
   na.X0 = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
   na.X1 = reinterpret_cast<__nv_bfloat16*>(ws + L.x1);
   na.lo_off = L.lo_off;
@@ -167,34 +232,56 @@ muon_status_t run_group_tail(const Layout& L, char* ws, int batch, const muon_vi
   if (fused) {
     // the last update's epilogue writes W (or the output) from its fp32 result
     FinalStore& f = na.fin;
-    f.mode = ap.mode == 0 ? 1 : 2;
-    f.rows = v.rows;
-    f.cols = v.cols;
-    f.tall = v.rows > v.cols;
-    f.dtype = ap.w_dtype;
-    f.w_ptrs = ap.w_ptrs;
-    f.w_ld = ap.row_stride;
-    f.out_base = ap.out_base;
-    f.wd_mask = ap.wd_mask;
+    f.mode = segs[0].ap.mode == 0 ? 1 : 2;
+    f.nseg = static_cast<int>(segs.size());
     f.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
-    f.decay_on = ap.decay_on;
-    f.lr_scale = ap.lr_scale;
+    for (size_t k = 0; k < segs.size(); ++k) {
+      const ApplyArgs& ap = segs[k].ap;
+      FinalSeg& g = f.seg[k];
+      g.begin = segs[k].begin;
+      g.rows = segs[k].view.rows;
+      g.cols = segs[k].view.cols;
+      g.tall = segs[k].view.rows > segs[k].view.cols;
+      g.dtype = ap.w_dtype;
+      g.w_ptrs = ap.w_ptrs;
+      g.w_ld = ap.row_stride;
+      g.out_base = ap.out_base;
+      g.wd_mask = ap.wd_mask;
+      g.decay_on = ap.decay_on;
+      g.lr_scale = ap.lr_scale;
+    }
   }
   e = run_ns_chain(na, st);
   if (e == cudaErrorNotSupported) return MUON_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return MUON_ERR_CUDA;
   if (fused) return MUON_OK;
 
-  ap.X = (iters % 2 == 0) ? na.X0 : na.X1;
-  ap.x_lo_off = L.lo_off;
-  ap.has_lo = ns_final_has_lo(iters, x3) ? 1 : 0;
-  ap.n_pad = L.n_pad;
-  ap.m_pad = L.m_pad;
-  ap.tall = v.rows > v.cols;
-  ap.parts = apply_parts(v.rows, v.cols);
-  ap.skip = reinterpret_cast<const uint8_t*>(ws + L.skip);
-  ap.oscale = (iters == 0 && normalize) ? reinterpret_cast<const float*>(ws + L.inv_s) : nullptr;
-  return cuda_status(launch_apply(ap, st));
+  for (const Segment& sg : segs) {
+    ApplyArgs ap = sg.ap;
+    const int64_t off = static_cast<int64_t>(sg.begin);
+    ap.X = ((iters % 2 == 0) ? na.X0 : na.X1) + off * L.n_pad * L.m_pad;
+    ap.x_lo_off = L.lo_off;
+    ap.has_lo = ns_final_has_lo(iters, x3) ? 1 : 0;
+    ap.n_pad = L.n_pad;
+    ap.m_pad = L.m_pad;
+    ap.tall = sg.view.rows > sg.view.cols;
+    ap.parts = apply_parts(sg.view.rows, sg.view.cols);
+    ap.skip = reinterpret_cast<const uint8_t*>(ws + L.skip) + off;
+    ap.oscale = (iters == 0 && normalize) ? reinterpret_cast<const float*>(ws + L.inv_s) + off
+                                          : nullptr;
+    const muon_status_t r = cuda_status(launch_apply(ap, st));
+    if (r != MUON_OK) return r;
+  }
+  return MUON_OK;
+}
+
+size_t step_workspace_bytes(const muon_group_t* groups, int n_groups, bool merge, bool x3) {
+  size_t need = kHeaderBytes;
+  for (const Chain& c : plan_chains(groups, n_groups, merge)) {
+    const Layout L = layout_for(c.batch, c.n_pad, c.m_pad, c.parts, x3);
+    if (L.total > need) need = L.total;
+  }
+  return need;
 }
 
 muon_status_t check_workspace(const void* ws, size_t bytes, size_t need) {
@@ -213,6 +300,7 @@ muon_status_t muon_ns_hybrid_schedule(muon_ns_schedule_t* out) {
   out->stages = kHybridStages;
   out->n_stages = 2;
   out->normalize = 1;
+  out->merge_groups = 0;
   out->prec = MUON_NS_BF16;
   return MUON_OK;
 }
@@ -254,18 +342,15 @@ muon_status_t muon_step_workspace_size(const muon_group_t* groups, int n_groups,
     return MUON_ERR_INVALID_ARG;
   std::vector<float> coeffs;
   int normalize = 1;
-  bool x3 = false;
-  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3);
+  bool x3 = false, merge = false;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3, &merge);
   if (s != MUON_OK) return s;
-  size_t need = kHeaderBytes;
   for (int i = 0; i < n_groups; ++i) {
     if (groups[i].batch < 1) return MUON_ERR_INVALID_ARG;
     s = check_view(groups[i].view);
     if (s != MUON_OK) return s;
-    const Layout L = layout_for(groups[i].batch, groups[i].view.rows, groups[i].view.cols, x3);
-    if (L.total > need) need = L.total;
   }
-  *bytes = need;
+  *bytes = step_workspace_bytes(groups, n_groups, merge, x3);
   return MUON_OK;
 }
 
@@ -286,8 +371,8 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
     return MUON_ERR_INVALID_ARG;
   std::vector<float> coeffs;
   int normalize = 1;
-  bool x3 = false;
-  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3);
+  bool x3 = false, merge = false;
+  muon_status_t s = expand_schedule(schedule, &coeffs, &normalize, &x3, &merge);
   if (s != MUON_OK) return s;
   for (int i = 0; i < n_groups; ++i) {
     const muon_group_t& g = groups[i];
@@ -320,50 +405,64 @@ muon_status_t muon_step_batched(const muon_group_t* groups, int n_groups,
     }
   }
 
-  for (int i = 0; i < n_groups; ++i) {
-    const muon_group_t& g = groups[i];
-    const Layout L = layout_for(g.batch, g.view.rows, g.view.cols, x3);
-    if (cudaMemsetAsync(ws + L.skip, 0, static_cast<size_t>(g.batch), st) != cudaSuccess)
+  const float decay_on = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
+  for (const Chain& c : plan_chains(groups, n_groups, merge)) {
+    const Layout L = layout_for(c.batch, c.n_pad, c.m_pad, c.parts, x3);
+    if (cudaMemsetAsync(ws + L.skip, 0, static_cast<size_t>(c.batch), st) != cudaSuccess)
       return MUON_ERR_CUDA;
-    PrepareArgs pa{};
-    pa.batch = g.batch;
-    pa.rows = g.view.rows;
-    pa.cols = g.view.cols;
-    pa.row_stride = g.view.row_stride;
-    pa.g_dtype = g.g_dtype;
-    pa.g_ptrs = g.g_ptrs;
-    pa.m_ptrs = g.m_ptrs;
-    pa.w_ptrs = g.w_ptrs;
-    pa.mode = hp->style == MUON_NESTEROV_SGD ? kPrepMomentumSgd : kPrepMomentumEma;
-    pa.nesterov = hp->nesterov;
-    pa.mu = hp->mu;
-    pa.ema_omb = 1.0 - beta;
-    pa.c_mom = static_cast<float>(c_mom);
-    pa.c_grad = static_cast<float>(c_grad);
-    pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0);
-    pa.x_lo_off = L.lo_off;
-    pa.n_pad = L.n_pad;
-    pa.m_pad = L.m_pad;
-    pa.tall = g.view.rows > g.view.cols;
-    pa.parts = L.parts;
-    pa.partials = reinterpret_cast<float*>(ws + L.partials);
-    pa.skip = reinterpret_cast<uint8_t*>(ws + L.skip);
-    pa.status = reinterpret_cast<uint32_t*>(ws);
-    if (launch_prepare(pa, st) != cudaSuccess) return MUON_ERR_CUDA;
+    std::vector<Segment> segs;
+    int begin = 0;
+    for (int gi : c.members) {
+      const muon_group_t& g = groups[gi];
+      const int64_t off = begin;
+      PrepareArgs pa{};
+      pa.batch = g.batch;
+      pa.rows = g.view.rows;
+      pa.cols = g.view.cols;
+      pa.row_stride = g.view.row_stride;
+      pa.g_dtype = g.g_dtype;
+      pa.g_ptrs = g.g_ptrs;
+      pa.m_ptrs = g.m_ptrs;
+      pa.w_ptrs = g.w_ptrs;
+      pa.mode = hp->style == MUON_NESTEROV_SGD ? kPrepMomentumSgd : kPrepMomentumEma;
+      pa.nesterov = hp->nesterov;
+      pa.mu = hp->mu;
+      pa.ema_omb = 1.0 - beta;
+      pa.c_mom = static_cast<float>(c_mom);
+      pa.c_grad = static_cast<float>(c_grad);
+      pa.X = reinterpret_cast<__nv_bfloat16*>(ws + L.x0) + off * L.n_pad * L.m_pad;
+      pa.x_lo_off = L.lo_off;
+      pa.n_pad = L.n_pad;
+      pa.m_pad = L.m_pad;
+      pa.tall = g.view.rows > g.view.cols;
+      pa.parts = prepare_parts(g.view.rows, g.view.cols, L.n_pad, L.m_pad);
+      pa.parts_stride = L.parts;
+      pa.partials = reinterpret_cast<float*>(ws + L.partials) + off * L.parts;
+      pa.skip = reinterpret_cast<uint8_t*>(ws + L.skip) + off;
+      pa.status = reinterpret_cast<uint32_t*>(ws);
+      if (launch_prepare(pa, st) != cudaSuccess) return MUON_ERR_CUDA;
 
-    const double scale = update_scale(g.view, hp->scale_mode, hp->gamma);
-    ApplyArgs ap{};
-    ap.batch = g.batch;
-    ap.rows = g.view.rows;
-    ap.cols = g.view.cols;
-    ap.row_stride = g.view.row_stride;
-    ap.mode = 0;
-    ap.w_dtype = g.w_dtype;
-    ap.w_ptrs = g.w_ptrs;
-    ap.wd_mask = g.wd_mask;
-    ap.decay_on = static_cast<float>(1.0 - static_cast<double>(hp->lr) * hp->weight_decay);
-    ap.lr_scale = static_cast<float>(static_cast<double>(hp->lr) * scale);
-    s = run_group_tail(L, ws, g.batch, g.view, coeffs, normalize, x3, ap, st);
+      Segment sg;
+      sg.begin = begin;
+      sg.batch = g.batch;
+      sg.parts = pa.parts;
+      sg.view = g.view;
+      ApplyArgs& ap = sg.ap;
+      ap.batch = g.batch;
+      ap.rows = g.view.rows;
+      ap.cols = g.view.cols;
+      ap.row_stride = g.view.row_stride;
+      ap.mode = 0;
+      ap.w_dtype = g.w_dtype;
+      ap.w_ptrs = g.w_ptrs;
+      ap.wd_mask = g.wd_mask;
+      ap.decay_on = decay_on;
+      ap.lr_scale = static_cast<float>(static_cast<double>(hp->lr) *
+                                       update_scale(g.view, hp->scale_mode, hp->gamma));
+      segs.push_back(sg);
+      begin += g.batch;
+    }
+    s = run_chain_tail(L, ws, c.batch, c.n, c.m, segs, coeffs, normalize, x3, st);
     if (s != MUON_OK) return s;
   }
   return MUON_OK;
@@ -379,7 +478,7 @@ muon_status_t newton_schulz_workspace_size(const muon_view_t* view, int batch,
   bool x3 = false;
   s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
-  *bytes = layout_for(batch, view->rows, view->cols, x3).total;
+  *bytes = layout_for(batch, *view, x3).total;
   return MUON_OK;
 }
 
@@ -409,7 +508,7 @@ muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_
   bool x3 = false;
   s = expand_schedule(schedule, &coeffs, &normalize, &x3);
   if (s != MUON_OK) return s;
-  const Layout L = layout_for(batch, view->rows, view->cols, x3);
+  const Layout L = layout_for(batch, *view, x3);
   s = check_workspace(workspace, workspace_bytes, L.total);
   if (s != MUON_OK) return s;
 
@@ -434,19 +533,25 @@ muon_status_t newton_schulz_batched(const void* x, muon_dtype_t xdt, const muon_
   pa.m_pad = L.m_pad;
   pa.tall = view->rows > view->cols;
   pa.parts = L.parts;
+  pa.parts_stride = L.parts;
   pa.partials = reinterpret_cast<float*>(ws + L.partials);
   pa.skip = reinterpret_cast<uint8_t*>(ws + L.skip);
   pa.status = reinterpret_cast<uint32_t*>(ws);
   if (launch_prepare(pa, st) != cudaSuccess) return MUON_ERR_CUDA;
 
-  ApplyArgs ap{};
-  ap.batch = batch;
-  ap.rows = view->rows;
-  ap.cols = view->cols;
-  ap.mode = 1;
-  ap.w_dtype = odt;
-  ap.out_base = out;
-  return run_group_tail(L, ws, batch, *view, coeffs, normalize, x3, ap, st);
+  Segment sg;
+  sg.begin = 0;
+  sg.batch = batch;
+  sg.parts = L.parts;
+  sg.view = *view;
+  sg.ap.batch = batch;
+  sg.ap.rows = view->rows;
+  sg.ap.cols = view->cols;
+  sg.ap.mode = 1;
+  sg.ap.w_dtype = odt;
+  sg.ap.out_base = out;
+  return run_chain_tail(L, ws, batch, wide_n(*view), wide_m(*view), {sg}, coeffs, normalize, x3,
+                        st);
 }
 
 muon_status_t muon_get_status(const void* workspace, muon_stream_t stream, uint32_t* flags) {

@@ -231,22 +231,30 @@ __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32])
 struct FinTile {
   void* base;        // W (mode 1) or the matrix's dense output (mode 2); nullptr = skip
   int64_t ld;
-  float decay;
+  float decay, lr_scale;
   int n_real, m_real;
+  bool tall, bf;     // W[j][i] holds wide element (i, j); bf16 storage
 };
 
+// Matrix b of the chain's batch: its segment's W (or output) and parameters.
 __device__ __forceinline__ FinTile fin_tile(const FinalStore& f, int b) {
+  int s = 0;
+  while (s + 1 < f.nseg && b >= f.seg[s + 1].begin) ++s;
+  const FinalSeg& g = f.seg[s];
+  const int bl = b - g.begin;
   FinTile t;
-  t.n_real = f.tall ? f.cols : f.rows;
-  t.m_real = f.tall ? f.rows : f.cols;
+  t.tall = g.tall != 0;
+  t.bf = (g.dtype == MUON_BF16);
+  t.n_real = t.tall ? g.cols : g.rows;
+  t.m_real = t.tall ? g.rows : g.cols;
   const bool muon = (f.mode == 1);
-  const int esz = (f.dtype == MUON_BF16) ? 2 : 4;
   t.base = f.skip[b] ? nullptr
-           : muon    ? f.w_ptrs[b]
-                     : static_cast<void*>(static_cast<char*>(f.out_base) +
-                                          static_cast<int64_t>(b) * f.rows * f.cols * esz);
-  t.ld = muon ? f.w_ld : f.cols;
-  t.decay = (muon && (f.wd_mask == nullptr || f.wd_mask[b])) ? f.decay_on : 1.f;
+           : muon    ? g.w_ptrs[bl]
+                     : static_cast<void*>(static_cast<char*>(g.out_base) +
+                                          static_cast<int64_t>(bl) * g.rows * g.cols * (t.bf ? 2 : 4));
+  t.ld = muon ? g.w_ld : g.cols;
+  t.decay = (muon && (g.wd_mask == nullptr || g.wd_mask[bl])) ? g.decay_on : 1.f;
+  t.lr_scale = g.lr_scale;
   return t;
 }
 
@@ -258,9 +266,9 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 __device__ __forceinline__ void fin_prefetch(const FinalStore& f, const FinTile& t, int row,
                                              int row0, int col_begin, int ncols, int lane) {
   if (t.base == nullptr || f.mode != 1) return;
-  const int esz = (f.dtype == MUON_BF16) ? 2 : 4;
+  const int esz = t.bf ? 2 : 4;
   const char* base = static_cast<const char*>(t.base);
-  if (!f.tall) {
+  if (!t.tall) {
     if (row >= t.n_real) return;
     const int c_end = min(col_begin + ncols, t.m_real);
     for (int j = col_begin; j < c_end; j += 128 / esz)
@@ -277,8 +285,8 @@ __device__ __forceinline__ void fin_prefetch(const FinalStore& f, const FinTile&
 __device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, int row, int col0,
                                          uint32_t (&w)[32]) {
   if (t.base == nullptr || f.mode != 1 || row >= t.n_real) return;
-  const bool bf = (f.dtype == MUON_BF16);
-  if (!f.tall) {
+  const bool bf = t.bf;
+  if (!t.tall) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = col0 + 8 * k;
@@ -318,12 +326,12 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
                                           const float (&v)[32], const uint32_t (&w)[32]) {
   if (t.base == nullptr || row >= t.n_real) return;
   const bool muon = (f.mode == 1);
-  const bool bf = (f.dtype == MUON_BF16);
+  const bool bf = t.bf;
   float o[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e)
-    o[e] = muon ? fmaf(-f.lr_scale, v[e], fin_w(bf, f.tall, w, e) * t.decay) : v[e];
-  if (!f.tall) {
+    o[e] = muon ? fmaf(-t.lr_scale, v[e], fin_w(bf, t.tall, w, e) * t.decay) : v[e];
+  if (!t.tall) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = col0 + 8 * k;

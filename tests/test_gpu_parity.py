@@ -314,3 +314,61 @@ def test_bounded_wait_times_out_and_context_survives():
     x = torch.randn(1, 128, 256, device=DEV)
     got = run_ns(x)
     assert rel_fro(f64(got[0]), oracle.newton_schulz(f64(x[0]))) <= NS_TOL
+
+
+# ---------------------------------------------------------------------------
+# groups sharing one Newton–Schulz chain (merge_groups)
+# ---------------------------------------------------------------------------
+HYBRID = [(8, (3.4445, -4.7750, 2.0315)), (2, (2.0, -1.5, 0.5))]
+
+
+def _merge_sets(seed):
+    """Groups: 3 wide 512x768 bf16, 2 tall 768x512 bf16, 2 of 256x384, 1 wide
+    512x768 fp32 W (four groups share the 512 x 768 wide shape)."""
+    specs = [(3, 512, 768, torch.bfloat16), (2, 768, 512, torch.bfloat16),
+             (2, 256, 384, torch.bfloat16), (1, 512, 768, torch.float32)]
+    out = []
+    for k, (b, r, c, wdt) in enumerate(specs):
+        W, G, M = workloads.random_case(seed + k, r, c, batch=b, w_dtype=wdt, m_scale=1.0)
+        out.append((W, G, M))
+    return out
+
+
+def _run_sets(sets, schedule, masks=None):
+    dev = [(W.to(DEV), G.to(DEV), M.to(DEV)) for W, G, M in sets]
+    groups = [m.Group.stacked(W, G, M, wd_mask=None if masks is None else masks[i])
+              for i, (W, G, M) in enumerate(dev)]
+    code, flags = step_once(groups, {}, schedule)
+    assert code == m.MUON_OK and flags == 0, (code, flags)
+    return [(W.cpu(), M.cpu()) for W, _, M in dev]
+
+
+@pytest.mark.parametrize("stages", [HYBRID, [(3, (3.4445, -4.7750, 2.0315))]],
+                         ids=["hybrid-fused-store", "three-iterations-apply-pass"])
+def test_merged_chains_equal_separate_chains_bitwise(stages):
+    """A tall and a wide group of one wide shape (and a same-shape fp32 group)
+    in one chain give bit-identical W and M to one chain per group; the
+    unmerged run is itself checked against the oracle."""
+    sets = _merge_sets(70)
+    masks = [[True, False, True], [False, True], None, [True]]
+    merged = _run_sets(sets, m.Schedule(stages, merge_groups=True), masks)
+    plain = _run_sets(sets, m.Schedule(stages), masks)
+    for (Wm, Mm), (Wp, Mp) in zip(merged, plain):
+        assert torch.equal(Wm, Wp) and torch.equal(Mm, Mp)
+    hp = hyper()
+    for gi, (W, G, M) in enumerate(sets):
+        for b in range(W.shape[0]):
+            decay_on = masks[gi] is None or masks[gi][b]
+            ref = oracle.muon_step(f64(W[b]), f64(G[b]), f64(M[b]), hp, decay=decay_on,
+                                   stages=stages)
+            check_w(f64(plain[gi][0][b]), ref["W"], hp, ref["scale"],
+                    bf16=W.dtype == torch.bfloat16)
+
+
+def test_more_groups_than_one_chain_holds():
+    """Five groups of one shape: chains of at most four groups."""
+    sets = [workloads.random_case(80 + k, 256, 512, batch=2) for k in range(5)]
+    merged = _run_sets(sets, m.Schedule(HYBRID, merge_groups=True))
+    plain = _run_sets(sets, m.Schedule(HYBRID))
+    for (Wm, Mm), (Wp, Mp) in zip(merged, plain):
+        assert torch.equal(Wm, Wp) and torch.equal(Mm, Mp)

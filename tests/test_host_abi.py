@@ -57,7 +57,7 @@ def test_struct_layouts_match_c(tmp_path):
         "O(muon_group_t,view)O(muon_group_t,w_ptrs)O(muon_group_t,wd_mask)"
         "O(muon_hparams_t,t)O(muon_hparams_t,lr)O(muon_view_t,row_stride)"
         "O(muon_view_t,fan_out_axis)O(muon_tensor_desc_t,w_dtype)"
-        "O(muon_ns_schedule_t,prec)return 0;}\n")
+        "O(muon_ns_schedule_t,prec)O(muon_ns_schedule_t,merge_groups)return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(prog),
                            "-o", str(exe)])
@@ -151,6 +151,30 @@ def test_workspace_size_layout(lib):
 def test_view_validation(lib, rows, cols, rs, want):
     code, _ = _ws_size([_group(rows, cols, rs)])
     assert code == want
+
+
+def test_merged_chains_workspace(lib):
+    """merge_groups: a 1024 x 4096 group and a 4096 x 1024 group share one
+    chain, so the workspace holds both batches at once; unmerged it holds the
+    larger group only.  Groups of another wide shape stay apart."""
+    merged = m.Schedule(oracle_hybrid(), merge_groups=True)
+    plain = m.Schedule(oracle_hybrid())
+    gs = [_group(1024, 4096, batch=8), _group(4096, 1024, batch=8), _group(512, 512, batch=2)]
+    c0, nb0 = _ws_size(gs, plain.ref)
+    c1, nb1 = _ws_size(gs, merged.ref)
+    one = _ws_size([_group(1024, 4096, batch=16)], plain.ref)[1]
+    assert c0 == c1 == m.MUON_OK
+    assert nb0 == _ws_size([_group(1024, 4096, batch=8)], plain.ref)[1]
+    assert nb1 == one
+    five = [_group(1024, 4096, batch=1) for _ in range(5)]      # chains of at most 4 groups
+    assert _ws_size(five, merged.ref)[1] == _ws_size([_group(1024, 4096, batch=4)], plain.ref)[1]
+    bad = m.Schedule(oracle_hybrid())
+    bad.c.merge_groups = 2
+    assert _ws_size(gs, bad.ref)[0] == m.MUON_ERR_INVALID_ARG
+
+
+def oracle_hybrid():
+    return [(8, (3.4445, -4.7750, 2.0315)), (2, (2.0, -1.5, 0.5))]
 
 
 def test_split_bf16_workspace_adds_lo_planes_of_s_and_p(lib):
