@@ -201,10 +201,11 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   }
 }
 
+// 32 bf16 of one row (64 bytes, 64-byte aligned in the workspace) as two
+// full-sector loads.
 __device__ __forceinline__ void load_raw4(const __nv_bfloat16* src, uint4 (&u)[4]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) u[q] = s[q];
+  ld_global_v8(src, u[0], u[1]);
+  ld_global_v8(src + 16, u[2], u[3]);
 }
 
 __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32]) {
@@ -490,13 +491,14 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
       }
       continue;
     }
+    // the row's 32 values as two full-sector stores per plane (workspace
+    // rows and planes are 256-byte aligned, col0 is a multiple of 32)
     __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
-    uint4* dst = reinterpret_cast<uint4*>(drow);
+    uint4 u[4], ul[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint4 u, ul;
-      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-      __nv_bfloat162* hl = reinterpret_cast<__nv_bfloat162*>(&ul);
+      __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[k]);
+      __nv_bfloat162* hl = reinterpret_cast<__nv_bfloat162*>(&ul[k]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float v0 = v[8 * k + 2 * e], v1 = v[8 * k + 2 * e + 1];
@@ -506,8 +508,12 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
           hl[e] = __floats2bfloat162_rn(v0 - f.x, v1 - f.y);
         }
       }
-      dst[k] = u;
-      if (lo_out) reinterpret_cast<uint4*>(drow + p.lo_off)[k] = ul;
+    }
+    st_global_v8(drow, u[0], u[1]);
+    st_global_v8(drow + 16, u[2], u[3]);
+    if (lo_out) {
+      st_global_v8(drow + p.lo_off, ul[0], ul[1]);
+      st_global_v8(drow + p.lo_off + 16, ul[2], ul[3]);
     }
     if (mirror) {
       // transposed copy: for each column e the warp's 32 lanes (32
