@@ -370,12 +370,18 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
 // applies the kernel's epilogue and stores.  The residual operand of the next
 // 32-column chunk is loaded while the current chunk is finished.  (Staging the
 // mirrored store through shared memory was slower: it competes with the
-// tensor core for shared-memory bandwidth.)  Returns false if the wait gave up.
-template <int BN, int EPI, bool SYM, int kChunksPerWarp = BN / 32>
+// tensor core for shared-memory bandwidth.)  With kTmaOut the direct
+// (untransposed) store goes through a per-warp 2 KB staging box per plane
+// (32 rows x 64 bytes, 64-byte swizzle) and one TMA store per box, so L2
+// sees whole 64-byte row segments instead of one request per lane.
+// Returns false if the wait gave up.
+template <int BN, int EPI, bool SYM, int kChunksPerWarp = BN / 32, bool kTmaOut = false>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_acc, int b, int tm,
                                               int tn, int q, int lane, uint64_t* tfull_bar,
                                               uint32_t parity, volatile int* abort_flag,
-                                              int c_begin = 0) {
+                                              int c_begin = 0, const CUtensorMap* tmO = nullptr,
+                                              const CUtensorMap* tmO2 = nullptr,
+                                              uint8_t* sbuf = nullptr) {
   const int row0 = tm * kBM + q * 32;
   const int row = row0 + lane;
   const bool mirror = SYM && (tn > tm / (BN / kBM));
@@ -491,9 +497,6 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
       }
       continue;
     }
-    // the row's 32 values as two full-sector stores per plane (workspace
-    // rows and planes are 256-byte aligned, col0 is a multiple of 32)
-    __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
     uint4 u[4], ul[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -509,11 +512,37 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
         }
       }
     }
-    st_global_v8(drow, u[0], u[1]);
-    st_global_v8(drow + 16, u[2], u[3]);
-    if (lo_out) {
-      st_global_v8(drow + p.lo_off, ul[0], ul[1]);
-      st_global_v8(drow + p.lo_off + 16, ul[2], ul[3]);
+    if constexpr (kTmaOut) {
+      // the previous chunk's boxes must have been read out of the staging
+      // buffers before they are overwritten
+      if (lane == 0) tma_store_wait_read0();
+      __syncwarp();
+      // row `lane` of the box, 16-byte unit k at unit k ^ ((lane >> 1) & 3)
+      // (the 64-byte swizzle; conflict-free for each quarter warp)
+      const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t off = static_cast<uint32_t>(lane) * 64u + 16u * (static_cast<uint32_t>(k) ^ sw);
+        *reinterpret_cast<uint4*>(sbuf + off) = u[k];
+        if (lo_out) *reinterpret_cast<uint4*>(sbuf + 2048 + off) = ul[k];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmO, sbuf, col0, row0, b);
+        if (lo_out) tma_store_3d(tmO2, sbuf + 2048, col0, row0, b);
+        tma_store_commit();
+      }
+    } else {
+      // the row's 32 values as two full-sector stores per plane (workspace
+      // rows and planes are 256-byte aligned, col0 is a multiple of 32)
+      __nv_bfloat16* drow = out + static_cast<int64_t>(row) * p.out_ld + col0;
+      st_global_v8(drow, u[0], u[1]);
+      st_global_v8(drow + 16, u[2], u[3]);
+      if (lo_out) {
+        st_global_v8(drow + p.lo_off, ul[0], ul[1]);
+        st_global_v8(drow + p.lo_off + 16, ul[2], ul[3]);
+      }
     }
     if (mirror) {
       // transposed copy: for each column e the warp's 32 lanes (32
@@ -764,14 +793,24 @@ constexpr int kEpiWarps2 = MUON_EPI2_WARPS;             // 4 or 8 (two per TMEM 
 constexpr int kGemmThreads2 = 64 + 32 * kEpiWarps2;
 constexpr uint32_t kHalfBytes2 = 128 * kBK * 2;      // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kStageBytes2 = 2 * kHalfBytes2;   // A + B half, per CTA
-constexpr size_t kSmemBytes2 = kStages2 * kStageBytes2 + 1024 + 256;
+// TMA-store staging: per epilogue warp one 2 KB box for the hi plane and one
+// for the lo plane (every kind but the last update, which writes W itself)
+constexpr uint32_t kStagingPerWarp2 = 4096;
+__host__ __device__ constexpr uint32_t staging_bytes2(int epi) {
+  return epi_kind(epi) == kEpiFinal ? 0u : kEpiWarps2 * kStagingPerWarp2;
+}
+__host__ __device__ constexpr size_t smem_bytes2(int epi) {
+  return kStages2 * kStageBytes2 + staging_bytes2(epi) + 1024 + 256;
+}
 
 template <bool B_MN, int EPI, bool SYM>
 __global__ void __launch_bounds__(kGemmThreads2, 1)
     k_ns_gemm2(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+               const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                const GemmParams p) {
   constexpr int BN = 256;
+  constexpr bool kTmaOut = staging_bytes2(EPI) != 0;
   constexpr uint32_t kTmemCols = kAccBufs2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, B_MN);
 
@@ -780,7 +819,8 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages2 * kHalfBytes2;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages2 * kStageBytes2);
+  uint8_t* staging = smem + kStages2 * kStageBytes2;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + staging_bytes2(EPI));
   uint64_t* empty = full + kStages2;
   uint64_t* tfull = empty + kStages2;
   uint64_t* tempty = tfull + 2;
@@ -929,9 +969,10 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
     for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
       decode_unit<BN, SYM, true>(p, t, rank, b, tm, tn);
-      if (!epilogue_tile<BN, EPI, SYM, kChunksPerWarp2>(
+      if (!epilogue_tile<BN, EPI, SYM, kChunksPerWarp2, kTmaOut>(
               p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
-              acc_phase, abort_flag, c_begin))
+              acc_phase, abort_flag, c_begin, &tmO, &tmO2,
+              staging + (warp - 2) * kStagingPerWarp2))
         break;
       tc_fence_before();
       __syncwarp();
@@ -941,6 +982,8 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
         acc_phase ^= 1u;
       }
     }
+    // every TMA store this warp issued completes before the CTA exits
+    if (kTmaOut && lane == 0) tma_store_wait_all0();
   }
 
   tc_fence_before();
@@ -1007,6 +1050,21 @@ bool map_mnmajor(CUtensorMap* m, const void* base, int batch, int K, int N) {
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Store boxes of a [batch][rows][cols] bf16 output: 32 columns (64 bytes,
+// the 64-byte swizzle span) x 32 rows, one box per epilogue warp and chunk.
+bool map_store(CUtensorMap* m, const void* base, int batch, int rows, int cols) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                                 static_cast<cuuint64_t>(rows) * cols * 2};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
                         const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
@@ -1055,11 +1113,12 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUt
 
 template <bool B_MN, int EPI, bool SYM>
 cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
-                         const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
-                         cudaStream_t st) {
+                         const CUtensorMap& tb2, const CUtensorMap& to, const CUtensorMap& to2,
+                         const GemmParams& p, double alg_flops, cudaStream_t st) {
   auto kern = k_ns_gemm2<B_MN, EPI, SYM>;
+  constexpr size_t kSmem = smem_bytes2(EPI);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes2));
+                                       static_cast<int>(kSmem));
   if (e != cudaSuccess) return e;
   const KernelKind kind = epi_kind(EPI) == kEpiGram ? kKindGram
                           : (epi_kind(EPI) == kEpiPoly ? kKindPoly : kKindUpdate);
@@ -1072,7 +1131,7 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CU
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.blockDim = dim3(kGemmThreads2);
-  cfg.dynamicSmemBytes = kSmemBytes2;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cfg.gridDim = dim3(2);
   int clusters = 0;
@@ -1087,7 +1146,7 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CU
     cfg.numAttrs = 2;
   }
   prof_begin(kind, st);
-  e = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, ta2, tb, tb2, to, to2, p);
   prof_end(kind, st, alg_flops, 0.0);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1100,14 +1159,16 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CU
 // their hi map in the lo slots (never read: the plane masks select hi only).
 struct OperandMaps {
   CUtensorMap k128, kbn, mn, k128_lo, kbn_lo, mn_lo;
+  CUtensorMap st, st_lo;  // 32 x 32 store boxes (pair-wide kernels' epilogue)
 };
 
 // Gram / polynomial: A and B are the same symmetric operand (X or S).
 template <int EPI>
-cudaError_t launch_sym(int bn, bool pair, const OperandMaps& A, const GemmParams& p, double f,
-                       cudaStream_t st) {
+cudaError_t launch_sym(int bn, bool pair, const OperandMaps& A, const OperandMaps& O,
+                       const GemmParams& p, double f, cudaStream_t st) {
   if (bn == 256 && pair && kUseTwoSm)
-    return launch_gemm2<false, EPI, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, p, f, st);
+    return launch_gemm2<false, EPI, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, O.st, O.st_lo, p,
+                                          f, st);
   if (bn == 256 && pair)
     return launch_gemm<256, false, EPI, true, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, p, f, st);
   if (bn == 256)
@@ -1118,9 +1179,10 @@ cudaError_t launch_sym(int bn, bool pair, const OperandMaps& A, const GemmParams
 // Update: A = P (K-major), B = X (MN-major).
 template <int EPI>
 cudaError_t launch_upd(int bn, bool pair, const OperandMaps& Pm, const OperandMaps& Xm,
-                       const GemmParams& p, double f, cudaStream_t st) {
+                       const OperandMaps& Om, const GemmParams& p, double f, cudaStream_t st) {
   if (bn == 256 && pair && kUseTwoSm)
-    return launch_gemm2<true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+    return launch_gemm2<true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, Om.st, Om.st_lo,
+                                          p, f, st);
   if (bn == 256 && pair)
     return launch_gemm<256, true, EPI, false, true>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
   if (bn == 256)
@@ -1132,14 +1194,17 @@ cudaError_t launch_upd(int bn, bool pair, const OperandMaps& Pm, const OperandMa
 
 bool map_square(OperandMaps* o, const __nv_bfloat16* hi, const __nv_bfloat16* lo, int batch, int n,
                 int bn) {
-  if (!map_kmajor(&o->k128, hi, batch, n, n, kBM) || !map_kmajor(&o->kbn, hi, batch, n, n, bn))
+  if (!map_kmajor(&o->k128, hi, batch, n, n, kBM) || !map_kmajor(&o->kbn, hi, batch, n, n, bn) ||
+      !map_store(&o->st, hi, batch, n, n))
     return false;
   if (lo == nullptr) {
     o->k128_lo = o->k128;
     o->kbn_lo = o->kbn;
+    o->st_lo = o->st;
     return true;
   }
-  return map_kmajor(&o->k128_lo, lo, batch, n, n, kBM) && map_kmajor(&o->kbn_lo, lo, batch, n, n, bn);
+  return map_kmajor(&o->k128_lo, lo, batch, n, n, kBM) &&
+         map_kmajor(&o->kbn_lo, lo, batch, n, n, bn) && map_store(&o->st_lo, lo, batch, n, n);
 }
 
 }  // namespace
@@ -1165,7 +1230,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
         !map_mnmajor(&X[i].mn, xb[i], batch, n, m) ||
         !map_kmajor(&X[i].k128_lo, lo, batch, n, m, kBM) ||
         !map_kmajor(&X[i].kbn_lo, lo, batch, n, m, bn_sq) ||
-        !map_mnmajor(&X[i].mn_lo, lo, batch, n, m))
+        !map_mnmajor(&X[i].mn_lo, lo, batch, n, m) || !map_store(&X[i].st, xb[i], batch, n, m) ||
+        !map_store(&X[i].st_lo, lo, batch, n, m))
       return cudaErrorInvalidValue;
   }
   if (!map_square(&S, a.A, x3 ? a.A + a.sq_lo_off : nullptr, batch, n, bn_sq) ||
@@ -1211,8 +1277,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     }
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
-    e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], g, f_gram, st)
-           : launch_sym<kEpiGram>(bn_sq, pair, X[cur], g, f_gram, st);
+    const OperandMaps& gram_out = (cc != 0.f) ? S : P;
+    e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], gram_out, g, f_gram, st)
+           : launch_sym<kEpiGram>(bn_sq, pair, X[cur], gram_out, g, f_gram, st);
     if (e != cudaSuccess) return e;
 
     if (cc != 0.f) {
@@ -1224,8 +1291,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.pdiag = x3 ? nullptr : a.pdiag;
       q.mscale = nullptr;
       if (x3) q.lo_in = 1;
-      e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, q, f_poly, st)
-             : launch_sym<kEpiPoly>(bn_sq, pair, S, q, f_poly, st);
+      e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, P, q, f_poly, st)
+             : launch_sym<kEpiPoly>(bn_sq, pair, S, P, q, f_poly, st);
       if (e != cudaSuccess) return e;
     }
 
@@ -1245,7 +1312,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       u.kplanes = x3_planes; u.a_lo_mask = x3_a_lo; u.b_lo_mask = x3_b_lo;
       u.lo_in = 1; u.lo_out = 1;
       u.ca = ca;
-      e = launch_upd<kEpiUpdate | kEpiX3>(bn_up, pair, P, X[cur], u, f_update, st);
+      e = launch_upd<kEpiUpdate | kEpiX3>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
       if (e != cudaSuccess) return e;
       continue;
     }
@@ -1258,9 +1325,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       u.fin = a.fin;
       u.lo_in = false;
       u.lo_out = false;
-      e = launch_upd<kEpiFinal>(bn_up, pair, P, X[cur], u, f_update, st);
+      e = launch_upd<kEpiFinal>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
     } else {
-      e = launch_upd<kEpiUpdate>(bn_up, pair, P, X[cur], u, f_update, st);
+      e = launch_upd<kEpiUpdate>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
     }
     if (e != cudaSuccess) return e;
   }

@@ -122,6 +122,32 @@ __device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const void
       : "memory");
 }
 
+// Tiled store of a shared-memory box to global memory (bulk-group
+// completion).  The issuing thread must have ordered the box's generic-proxy
+// writes before it with fence.proxy.async (see fence_proxy_async_smem).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1),
+               "r"(c2)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk stores have finished reading
+// shared memory (the source boxes may be overwritten).
+__device__ __forceinline__ void tma_store_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk stores are complete.
+__device__ __forceinline__ void tma_store_wait_all0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
