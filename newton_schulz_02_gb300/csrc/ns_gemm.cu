@@ -34,9 +34,9 @@
 // Precision.  Operands are bf16 with fp32 accumulation; S and P are stored
 // as bf16; the iterate is stored as two bf16 planes X = hi + lo with
 // lo = bf16(x - hi) for the first kLoIters iterations and as hi alone after
-// that.  The exact X term of the update reads hi + lo.  In the first
-// kResidualIters iterations the product also reads both planes (P hi + P lo,
-// one K-loop over the two planes); later iterations read hi.
+// that.  The exact X term of the update reads hi + lo; the product P X
+// reads hi only, and the epilogue adds back the shift's share of the
+// dropped P lo, (a - 1) lo, exactly in fp32.
 // Why: when a few singular directions dominate the entries (a low-rank
 // spike in the gradient), rounding X to bf16 puts noise the size of the
 // large entries into the small directions, which the fast stage multiplies
@@ -44,10 +44,16 @@
 // still small, the product need the residual.  Writing the update as
 // X + P X with the a - 1 shift inside P keeps the product's coefficient small
 // on directions that have converged (a + b + c - 1: -0.30 in the fast stage,
-// 0 in the stable stage), so dropping lo from the product in later
-// iterations costs little; written as a X + (b S + c S^2) X, converged
-// directions would cancel 3.44 X against -2.74 X and amplify the dropped
-// residual about ninefold.
+// 0 in the stable stage), so dropping lo from the product costs little
+// there; on the directions that are still small P is (a - 1) I plus terms
+// of order sigma^2, so (a - 1) lo is nearly all of P lo, and it costs no
+// tensor work.  (Written as a X + (b S + c S^2) X, converged directions would
+// cancel 3.44 X against -2.74 X and amplify the dropped residual about
+// ninefold.)  Reading lo in the product instead (a second K-loop over the lo
+// plane) doubles the first updates' tensor work for a result no closer to
+// float64 on the spiky, row-scaled and Gaussian sets (worst relative error
+// 7.7e-3 against 5.5e-3 with the shift share; 4.3e-3 against 5.0e-3 on the
+// Student-t set).
 //
 // Split-bf16 precision (kEpiX3, MUON_NS_BF16X3): S, P and X are all stored
 // as hi + lo planes and every GEMM runs one K-loop over three plane pairs,
@@ -71,7 +77,7 @@ namespace muon {
 namespace {
 
 constexpr int kBM = 128;  // tile rows (TMEM lanes)
-constexpr int kResidualIters = 2;  // iterations whose product also reads the lo plane
+constexpr int kResidualIters = 0;  // iterations whose product also reads the lo plane
 constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
 constexpr bool kUsePairs = true;   // 2-CTA clusters sharing the B tile (see k_ns_gemm)
 #ifndef MUON_PDL
@@ -119,6 +125,8 @@ struct GemmParams {
   int lo_in, lo_out;  // update (any kind with kEpiX3): read aux's lo plane / write out's lo plane
   float ca, cb, cc;
   float cd;         // added on the diagonal (Gram when c == 0, Poly): a - 1
+  float clo;        // update whose product reads X hi only: coefficient of the
+                    // lo plane added in the epilogue (a - 1, the shift's share of P lo)
   int kplanes;      // K-loop over 1..3 operand planes; plane p reads A's lo plane
   int a_lo_mask;    // (tmA2) if bit p of a_lo_mask is set, else its hi plane
   int b_lo_mask;    // (tmA), and likewise B from tmB2 / tmB
@@ -235,6 +243,7 @@ struct FinTile {
   float decay, lr_scale;
   int n_real, m_real;
   bool tall, bf;     // W[j][i] holds wide element (i, j); bf16 storage
+  bool v8;           // wide rows 32-byte aligned: 256-bit accesses
 };
 
 // Matrix b of the chain's batch: its segment's W (or output) and parameters.
@@ -254,6 +263,9 @@ __device__ __forceinline__ FinTile fin_tile(const FinalStore& f, int b) {
                      : static_cast<void*>(static_cast<char*>(g.out_base) +
                                           static_cast<int64_t>(bl) * g.rows * g.cols * (t.bf ? 2 : 4));
   t.ld = muon ? g.w_ld : g.cols;
+  const int esz = t.bf ? 2 : 4;
+  t.v8 = !t.tall && t.base != nullptr && (reinterpret_cast<uintptr_t>(t.base) & 31u) == 0 &&
+         ((t.ld * esz) & 31) == 0;
   t.decay = (muon && (g.wd_mask == nullptr || g.wd_mask[bl])) ? g.decay_on : 1.f;
   t.lr_scale = g.lr_scale;
   return t;
@@ -288,11 +300,33 @@ __device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, 
   if (t.base == nullptr || f.mode != 1 || row >= t.n_real) return;
   const bool bf = t.bf;
   if (!t.tall) {
+    // whole 32-byte sectors where the row allows (m_real is a multiple of 8)
+    const int64_t roff = static_cast<int64_t>(row) * t.ld;
+    if (t.v8 && col0 + 32 <= t.m_real) {
+      if (bf) {
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(t.base) + roff + col0;
+        uint4 a, b, c, d;
+        ld_global_v8(src, a, b);
+        ld_global_v8(src + 16, c, d);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        w[8] = c.x; w[9] = c.y; w[10] = c.z; w[11] = c.w; w[12] = d.x; w[13] = d.y; w[14] = d.z; w[15] = d.w;
+      } else {
+        const float* src = static_cast<const float*>(t.base) + roff + col0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 a, b;
+          ld_global_v8(src + 8 * k, a, b);
+          w[8 * k] = a.x; w[8 * k + 1] = a.y; w[8 * k + 2] = a.z; w[8 * k + 3] = a.w;
+          w[8 * k + 4] = b.x; w[8 * k + 5] = b.y; w[8 * k + 6] = b.z; w[8 * k + 7] = b.w;
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = col0 + 8 * k;
       if (j >= t.m_real) continue;  // m_real is a multiple of 8
-      const int64_t off = static_cast<int64_t>(row) * t.ld + j;
+      const int64_t off = roff + j;
       if (bf) {
         const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(t.base) + off);
         w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
@@ -333,11 +367,36 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
   for (int e = 0; e < 32; ++e)
     o[e] = muon ? fmaf(-t.lr_scale, v[e], fin_w(bf, t.tall, w, e) * t.decay) : v[e];
   if (!t.tall) {
+    const int64_t roff = static_cast<int64_t>(row) * t.ld;
+    if (t.v8 && col0 + 32 <= t.m_real) {
+      if (bf) {
+        uint4 u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u[k]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(o[8 * k + 2 * e], o[8 * k + 2 * e + 1]);
+        }
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(t.base) + roff + col0;
+        st_global_v8(dst, u[0], u[1]);
+        st_global_v8(dst + 16, u[2], u[3]);
+      } else {
+        float* dst = static_cast<float*>(t.base) + roff + col0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_global_v8(dst + 8 * k,
+                       make_uint4(__float_as_uint(o[8 * k]), __float_as_uint(o[8 * k + 1]),
+                                  __float_as_uint(o[8 * k + 2]), __float_as_uint(o[8 * k + 3])),
+                       make_uint4(__float_as_uint(o[8 * k + 4]), __float_as_uint(o[8 * k + 5]),
+                                  __float_as_uint(o[8 * k + 6]), __float_as_uint(o[8 * k + 7])));
+      }
+      return;
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int j = col0 + 8 * k;
       if (j >= t.m_real) continue;
-      const int64_t off = static_cast<int64_t>(row) * t.ld + j;
+      const int64_t off = roff + j;
       if (bf) {
         uint4 u;
         __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
@@ -464,12 +523,16 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
           for (int e = 0; e < 32; ++e)
             v[e] = fmaf(p.ca, x[e] + xl[e], __uint_as_float(r[e])) * ms;
         } else {
-          // P = bS + cS^2 + (a - 1) I; its diagonal's rounding residual d
+          // P = bS + cS^2 + (a - 1) I; its diagonal's rounding residual d;
+          // when the product read X hi only, P lo is approximated by its
+          // shift part (a - 1) lo (the rest, (bS + cS^2) lo, is small on the
+          // directions that are still small and decays on converged ones)
           const float d = d_row;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const float xe = x[e] + xl[e];
-            v[e] = fmaf(d, xe, xe + __uint_as_float(r[e])) * ms;   // X + P X + d_row X
+            // X + P X + d_row X (+ clo X_lo)
+            v[e] = fmaf(d, xe, fmaf(p.clo, xl[e], xe + __uint_as_float(r[e]))) * ms;
           }
         }
       }
@@ -1320,6 +1383,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.b_lo_mask = (u.kplanes == 2) ? 0b10 : 0;
     u.lo_in = it < kLoIters;
     u.lo_out = it + 1 < kLoIters;
+    u.clo = (u.kplanes == 1 && u.lo_in) ? ca - 1.f : 0.f;
     if ((it + 1 == a.iters) && a.fin.mode != 0) {
       // the last update writes W (or the output); it has no lo plane
       u.fin = a.fin;
