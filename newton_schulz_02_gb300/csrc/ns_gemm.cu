@@ -460,6 +460,9 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
   }
   constexpr bool kFin = (K == kEpiFinal);
+  // symmetric kinds of the bf16 precision: the mirrored copy goes out as a
+  // TMA store of a transposed box too
+  constexpr bool kMirrorTma = kTmaOut && SYM && !kX3;
   FinTile ft{};
   uint32_t w_cur[32], w_nxt[32];
   if (kFin) {
@@ -589,11 +592,32 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
         *reinterpret_cast<uint4*>(sbuf + off) = u[k];
         if (lo_out) *reinterpret_cast<uint4*>(sbuf + 2048 + off) = ul[k];
       }
+      if (kMirrorTma && mirror) {
+        // transposed box in the second buffer (free: symmetric kinds of the
+        // bf16 precision write no lo plane).  Box row c holds tile column
+        // col0 + c over the warp's 32 rows.  Word w of a lane packs its
+        // columns 2w, 2w+1; after one exchange with the neighbouring lane,
+        // an even lane writes (its, neighbour's) value of column 2w and an
+        // odd lane (neighbour's, its) value of column 2w + 1: each store
+        // instruction fills two 64-byte box rows.
+        const uint32_t* wv = reinterpret_cast<const uint32_t*>(u);
+        const uint32_t odd = static_cast<uint32_t>(lane) & 1u;
+        const uint32_t rbyte = 2u * (static_cast<uint32_t>(lane) & ~1u);
+#pragma unroll
+        for (int w = 0; w < 16; ++w) {
+          const uint32_t x = __shfl_xor_sync(0xffffffffu, wv[w], 1);
+          const uint32_t word = odd ? __byte_perm(x, wv[w], 0x7632) : __byte_perm(wv[w], x, 0x5410);
+          const uint32_t c = 2u * static_cast<uint32_t>(w) + odd;
+          const uint32_t off = c * 64u + ((((rbyte >> 4) ^ ((c >> 1) & 3u))) << 4) + (rbyte & 15u);
+          *reinterpret_cast<uint32_t*>(sbuf + 2048 + off) = word;
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         tma_store_3d(tmO, sbuf, col0, row0, b);
         if (lo_out) tma_store_3d(tmO2, sbuf + 2048, col0, row0, b);
+        if (kMirrorTma && mirror) tma_store_3d(tmO, sbuf + 2048, row0, col0, b);
         tma_store_commit();
       }
     } else {
@@ -607,7 +631,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
         st_global_v8(drow + p.lo_off + 16, ul[2], ul[3]);
       }
     }
-    if (mirror) {
+    if (mirror && !kMirrorTma) {
       // transposed copy: for each column e the warp's 32 lanes (32
       // consecutive rows) store 64 contiguous bytes of row col0 + e
 #pragma unroll
