@@ -137,6 +137,7 @@ struct GemmParams {
   uint32_t* status;
   uint64_t timeout_ns;
   FinalStore fin;   // update, last iteration: fused scale / decay / store
+  int reverse;      // walk the units from the last matrix to the first
 };
 
 // Tile t -> (matrix, tile row, tile column).  For symmetric outputs only the
@@ -170,6 +171,7 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& b, 
 template <int BN, bool SYM, bool PAIR>
 __device__ __forceinline__ void decode_unit(const GemmParams& p, int t, uint32_t rank, int& b,
                                             int& tm, int& tn) {
+  if (p.reverse) t = p.total_tiles - 1 - t;
   if (!PAIR) {
     decode_tile<BN, SYM>(p, t, b, tm, tn);
     return;
@@ -1337,6 +1339,10 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   // split-bf16: planes (hi, hi), (hi, lo), (lo, hi) of (A, B)
   const int x3_planes = 3, x3_a_lo = 0b100, x3_b_lo = 0b010;
 
+  // Consecutive launches walk the batch in opposite directions, so that each
+  // starts on the matrices its predecessor wrote last (still in L2); the
+  // first Gram follows the prepare pass, which writes the batch in order.
+  int launch = 0;
   for (int it = 0; it < a.iters; ++it) {
     const float ca = a.coeffs[3 * it], cb = a.coeffs[3 * it + 1], cc = a.coeffs[3 * it + 2];
     const int cur = it & 1;
@@ -1364,6 +1370,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     }
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
+    g.reverse = (launch++ & 1) == 0;
     const OperandMaps& gram_out = (cc != 0.f) ? S : P;
     e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], gram_out, g, f_gram, st)
            : launch_sym<kEpiGram>(bn_sq, pair, X[cur], gram_out, g, f_gram, st);
@@ -1377,6 +1384,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       q.cb = cb; q.cc = cc; q.cd = x3 ? 0.f : ca - 1.f;
       q.pdiag = x3 ? nullptr : a.pdiag;
       q.mscale = nullptr;
+      q.reverse = (launch++ & 1) == 0;
       if (x3) q.lo_in = 1;
       e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, P, q, f_poly, st)
              : launch_sym<kEpiPoly>(bn_sq, pair, S, P, q, f_poly, st);
@@ -1395,6 +1403,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     u.pdiag_in = a.pdiag; u.pdiag_bstride = n;
     u.mscale = first ? a.inv_s : nullptr;
     u.status = a.status; u.timeout_ns = a.timeout_ns;
+    u.reverse = (launch++ & 1) == 0;
     if (x3) {
       u.kplanes = x3_planes; u.a_lo_mask = x3_a_lo; u.b_lo_mask = x3_b_lo;
       u.lo_in = 1; u.lo_out = 1;
