@@ -435,37 +435,69 @@ def run_ours(args):
         e2e = {"value": None, "unit": "params/s", "skipped": "multi-GB device-drawn set; the "
                "end-to-end leg runs on the stacked workload"}
     elif args.e2e_steps > 0:
+        # Pipelined the way a training loop fed from host memory runs: step
+        # i's gradient upload (its own copy stream, two device slots) overlaps
+        # step i - 1, and step i's W goes to the host from a device snapshot
+        # taken on the compute stream right after the step, while step i + 1
+        # runs.  Every step's uploads and downloads lie inside the timed region
+        # (the first upload waits for its start, its end waits for the last
+        # download); each step's status word is saved on the device and all are
+        # read back and checked at the end.
+        n_e = args.e2e_steps
         Gh = [g.pin_memory() for g in wl["grads"]]
-        Gslot = torch.empty_like(Gd[0])
+        Gslots = [torch.empty_like(Gd[0]) for _ in range(2)]
+        Wsnap = torch.empty_like(Wd)
         Wh = torch.empty(Wd.shape, dtype=Wd.dtype).pin_memory()
-        eg = make_groups(m, wl, Wd, Md, [Gslot])[0]
-        flags_h = []
+        egs = [make_groups(m, wl, Wd, Md, [g])[0] for g in Gslots]
+        status_word = ws[:4].view(torch.int32)
+        flags_d = torch.zeros(n_e, dtype=torch.int32, device=dev)
+        flags_h = torch.empty(n_e, dtype=torch.int32).pin_memory()
+        s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_g = [torch.cuda.Event() for _ in range(n_e)]
+        ev_done = [torch.cuda.Event() for _ in range(n_e)]
+        ev_out = [torch.cuda.Event() for _ in range(n_e)]
         for i in range(2):
-            Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
-            m.muon_step_batched(eg, hp, ws, sched)
+            Gslots[i].copy_(Gh[i % len(Gh)], non_blocking=True)
+            m.muon_step_batched(egs[i], hp, ws, sched)
         torch.cuda.synchronize()
         barrier()
         t0 = time.perf_counter()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(args.e2e_steps):
-            Gslot.copy_(Gh[i % len(Gh)], non_blocking=True)
-            m.muon_step_batched(eg, hp, ws, sched)
-            Wh.copy_(Wd, non_blocking=True)
-            flags_h.append(m.muon_get_status(ws))
+        for i in range(n_e):
+            slot = i % 2
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])  # slot free again
+                Gslots[slot].copy_(Gh[i % len(Gh)], non_blocking=True)
+                ev_g[i].record(s_h2d)
+            stream.wait_event(ev_g[i])
+            m.muon_step_batched(egs[slot], hp, ws, sched)
+            flags_d[i:i + 1].copy_(status_word)
+            if i > 0:
+                stream.wait_event(ev_out[i - 1])  # the snapshot has left for the host
+            Wsnap.copy_(Wd)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[i])
+                Wh.copy_(Wsnap, non_blocking=True)
+                ev_out[i].record(s_d2h)
+        stream.wait_event(ev_out[n_e - 1])
+        flags_h.copy_(flags_d, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        if any(c != m.MUON_OK or f for c, f in flags_h):
+        if int(flags_h.abs().sum()) != 0:
             raise RuntimeError("device status set during the end-to-end steps")
-        e2e = {"value": job_value(args.e2e_steps, P, world, e_ms), "unit": "params/s",
-               "h2d_bytes_per_step": int(Gslot.numel() * Gslot.element_size()),
+        e2e = {"value": job_value(n_e, P, world, e_ms), "unit": "params/s",
+               "h2d_bytes_per_step": int(Gslots[0].numel() * Gslots[0].element_size()),
                "d2h_bytes_per_step": int(Wh.numel() * Wh.element_size() + 4),
-               "steps": args.e2e_steps, "wall_s": round(wall, 4),
-               "path": "pinned host G -> device, muon_step_batched, device W -> pinned host, "
-                       "status word read (synchronising) every step"}
+               "steps": n_e, "wall_s": round(wall, 4),
+               "path": "pinned host G -> device (copy stream, overlapping the previous step), "
+                       "muon_step_batched, W snapshot on the device -> pinned host (copy "
+                       "stream, overlapping the next step); each step's status word saved "
+                       "on the device and checked after the last step"}
 
     if rank != 0:
         if world > 1:
@@ -638,28 +670,55 @@ def run_adamw(args):
 
     e2e = None
     if args.e2e_steps > 0:
-        # pinned host gradients in, updated W out, every step
+        # pinned host gradients in, updated W out, every step; pipelined as in
+        # the Muon leg: uploads into two device gradient slots on one copy
+        # stream, W snapshots on the device, downloads on another copy stream
+        steps = max(1, min(args.e2e_steps, 5))
         Gh = [g.cpu().pin_memory() for g in G]
         Wh = [torch.empty(w.shape, dtype=w.dtype).pin_memory() for w in W]
-        steps = max(1, min(args.e2e_steps, 5))
+        Gslots = [G, [torch.empty_like(g) for g in G]]
+        Wsnap = [torch.empty_like(w) for w in W]
+        sgroups = [m.adamw_groups(W, gs, M, V, wd_mask=part["wd_mask"]) for gs in Gslots]
+        s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_g = [torch.cuda.Event() for _ in range(steps)]
+        ev_done = [torch.cuda.Event() for _ in range(steps)]
+        ev_out = [torch.cuda.Event() for _ in range(steps)]
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
-            for g, gh in zip(G, Gh):
-                g.copy_(gh, non_blocking=True)
-            m.muon_adamw_step(groups, m.adamw_hparams(t=t), flags)
+        for i in range(steps):
+            slot = i % 2
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])
+                for g, gh in zip(Gslots[slot], Gh):
+                    g.copy_(gh, non_blocking=True)
+                ev_g[i].record(s_h2d)
+            stream.wait_event(ev_g[i])
+            m.muon_adamw_step(sgroups[slot], m.adamw_hparams(t=t), flags)
             t += 1
-            for w, wh in zip(W, Wh):
-                wh.copy_(w, non_blocking=True)
+            if i > 0:
+                stream.wait_event(ev_out[i - 1])
+            for ws_, w in zip(Wsnap, W):
+                ws_.copy_(w)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[i])
+                for wh, ws_ in zip(Wh, Wsnap):
+                    wh.copy_(ws_, non_blocking=True)
+                ev_out[i].record(s_d2h)
+        stream.wait_event(ev_out[steps - 1])
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        if int(flags.item()) != 0:
+            raise RuntimeError(f"device flags {int(flags.item()):#x}")
         e2e = {"value": job_value(steps, P, world, e_ms), "unit": "params/s",
                "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in G)),
                "d2h_bytes_per_step": int(sum(w.numel() * w.element_size() for w in W)),
-               "steps": steps, "path": "pinned host G -> device, muon_adamw_step, device W -> "
-                                        "pinned host"}
+               "steps": steps, "path": "pinned host G -> device (copy stream, overlapping the "
+                                        "previous step), muon_adamw_step, W snapshot on the "
+                                        "device -> pinned host (copy stream, overlapping the "
+                                        "next step)"}
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
