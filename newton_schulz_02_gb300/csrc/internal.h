@@ -135,6 +135,7 @@ struct NsChainArgs {
   int x3;               // split-bf16 precision: S and P carry lo planes at +sq_lo_off
   int64_t sq_lo_off;
   FinalStore fin;       // fused into the last iteration when fin.mode != 0
+  float* partial;       // split-K Gram slices, gram_ksplit(...) * batch * n_pad^2 fp32, or nullptr
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -193,6 +194,11 @@ bool ns_final_has_lo(int iters, bool x3);
 // (NsChainArgs::fin); otherwise the iterate stays in the workspace for the
 // separate last pass.
 bool ns_final_fused(int iters, bool x3);
+
+// K-slices of the Gram of a chain of padded wide shape n_pad x m_pad (1 =
+// unsplit); a function of the shape alone, so that a matrix's result does not
+// depend on the batch it is in.
+int gram_ksplit(int n_pad, int m_pad, bool x3);
 
 // Runs the whole chain; the final iterate is left in X0 if the number of
 // iterations is even, else in X1.  Returns cudaErrorNotSupported when the

@@ -46,6 +46,8 @@ struct Layout {
   int64_t lo_off = 0;     // elements from an iterate's hi plane to its lo plane
   int64_t sq_lo_off = 0;  // split-bf16: from S's (P's) hi plane to its lo plane
   size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
+  size_t kslices = 0;     // split-K Gram slices (fp32), when gram_ksplit(...) > 1
+  int ksplit = 1;
 };
 
 int wide_n(const muon_view_t& v) { return v.rows < v.cols ? v.rows : v.cols; }
@@ -74,6 +76,11 @@ Layout layout_for(int batch, int n_pad, int m_pad, int parts, bool x3) {
   L.partials = off; off += align256(static_cast<size_t>(batch) * L.parts * 4);
   L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
   L.skip = off; off += align256(static_cast<size_t>(batch));
+  L.ksplit = gram_ksplit(n_pad, m_pad, x3);
+  if (L.ksplit > 1) {
+    L.kslices = off;
+    off += align256(static_cast<size_t>(L.ksplit) * batch * L.n_pad * L.n_pad * 4);
+  }
   L.total = off;
   return L;
 }
@@ -228,6 +235,7 @@ muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
   na.timeout_ns = g_timeout_ns.load();
   na.x3 = x3 ? 1 : 0;
   na.sq_lo_off = L.sq_lo_off;
+  na.partial = L.ksplit > 1 ? reinterpret_cast<float*>(ws + L.kslices) : nullptr;
   const bool fused = ns_final_fused(iters, x3);
   if (fused) {
     // the last update's epilogue writes W (or the output) from its fp32 result

@@ -138,6 +138,9 @@ struct GemmParams {
   uint64_t timeout_ns;
   FinalStore fin;   // update, last iteration: fused scale / decay / store
   int reverse;      // walk the units from the last matrix to the first
+  int ksplit;       // Gram split into ksplit K-slices (1-CTA kernel): unit t is slice
+                    // t % ksplit of tile t / ksplit; 0 or 1 = whole K
+  float* partial;   // split-K: fp32 [ksplit][batch][n][n] raw accumulators
 };
 
 // Tile t -> (matrix, tile row, tile column).  For symmetric outputs only the
@@ -442,7 +445,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
                                               uint32_t parity, volatile int* abort_flag,
                                               int c_begin = 0, const CUtensorMap* tmO = nullptr,
                                               const CUtensorMap* tmO2 = nullptr,
-                                              uint8_t* sbuf = nullptr) {
+                                              uint8_t* sbuf = nullptr, int slice = 0) {
   const int row0 = tm * kBM + q * 32;
   const int row = row0 + lane;
   const bool mirror = SYM && (tn > tm / (BN / kBM));
@@ -497,6 +500,17 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     tmem_ld_32x32b_x32(t_row + c * 32, r);
     tmem_ld_wait(r);
     const int col0 = tn * BN + c * 32;
+    if (K == kEpiGram && !kX3 && p.ksplit > 1) {
+      // split-K: this slice's raw fp32 sums (k_gram_reduce finishes the Gram)
+      float* dst = p.partial + ((static_cast<int64_t>(slice) * (p.total_tiles / p.ksplit /
+                                                                 p.tiles_per_matrix) +
+                                 b) * p.M + row) * p.M + col0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_global_v8(dst + 8 * k, make_uint4(r[8 * k], r[8 * k + 1], r[8 * k + 2], r[8 * k + 3]),
+                     make_uint4(r[8 * k + 4], r[8 * k + 5], r[8 * k + 6], r[8 * k + 7]));
+      continue;
+    }
     float v[32];
     if (K == kEpiGram) {
       const float s2 = ms * ms * p.cb;
@@ -721,6 +735,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   griddep_wait();  // the previous kernel's outputs are this kernel's inputs
   const int nkb = p.K / kBK;
   const int nkb_total = nkb * p.kplanes;
+  // split-K (symmetric Grams with few tiles): unit t is K-slice t % nsplit of tile t / nsplit
+  const int nsplit = p.ksplit > 1 ? p.ksplit : 1;
+  const int nkb_run = nkb_total / nsplit;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -730,9 +747,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         int b, tm, tn;
-        decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
-        int plane = 0, kk = 0;                     // operand plane, k-block within it
-        for (int kb = 0; kb < nkb_total; ++kb) {
+        decode_unit<BN, SYM, PAIR>(p, t / nsplit, rank, b, tm, tn);
+        int plane = 0, kk = (t % nsplit) * nkb_run;    // operand plane, k-block within it
+        for (int kb = 0; kb < nkb_run; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -791,7 +808,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nkb_total; ++kb) {
+        for (int kb = 0; kb < nkb_run; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -840,9 +857,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
-      decode_unit<BN, SYM, PAIR>(p, t, rank, b, tm, tn);
+      decode_unit<BN, SYM, PAIR>(p, t / nsplit, rank, b, tm, tn);
       if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
-                                       q, lane, &tfull[acc], acc_phase, abort_flag))
+                                       q, lane, &tfull[acc], acc_phase, abort_flag, 0, nullptr,
+                                       nullptr, nullptr, t % nsplit))
         break;
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -1086,6 +1104,66 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
 }
 
 
+// ---- split-K Gram: the sum of the K-slices and the Gram epilogue ---------
+// One thread per 4 consecutive columns of a row; the slices are added in
+// index order, so the result depends on the matrix alone.  Same epilogue as
+// the unsplit Gram: scale (1/||X||^2 on the first iteration, b when the Gram
+// writes P directly), the (a - 1) shift on the diagonal with its fp32
+// rounding residual, bf16 store, transposed copy of off-diagonal super-blocks.
+struct GramReduceArgs {
+  const float* partial;   // [ksplit][batch][n][n]
+  int ksplit, batch, n, bn;
+  __nv_bfloat16* out;     // [batch][n][n]
+  float cb, cd;
+  const float* mscale;    // [batch] or nullptr
+  float* pdiag;           // [batch][n] or nullptr
+};
+
+__global__ void __launch_bounds__(256) k_gram_reduce(const GramReduceArgs a) {
+  griddep_wait();
+  const int q = a.n / 4;
+  const int64_t per_mat = static_cast<int64_t>(a.n) * q;
+  const int64_t total = per_mat * a.batch;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(i / per_mat);
+    const int rem = static_cast<int>(i - static_cast<int64_t>(b) * per_mat);
+    const int row = rem / q;
+    const int col = (rem - row * q) * 4;
+    const int sr = row / a.bn, sc = col / a.bn;
+    if (sc < sr) continue;  // lower super-blocks are written as mirrors
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int sl = 0; sl < a.ksplit; ++sl) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+          a.partial + ((static_cast<int64_t>(sl) * a.batch + b) * a.n + row) * a.n + col));
+      acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+    }
+    const float ms = a.mscale != nullptr ? a.mscale[b] : 1.f;
+    const float f = ms * ms * a.cb;
+    __nv_bfloat16 h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float v = acc[e] * f;
+      if (row == col + e) {
+        v += a.cd;
+        if (a.pdiag != nullptr)
+          a.pdiag[static_cast<int64_t>(b) * a.n + row] = v - __bfloat162float(__float2bfloat16_rn(v));
+      }
+      h[e] = __float2bfloat16_rn(v);
+    }
+    __nv_bfloat16* o = a.out + static_cast<int64_t>(b) * a.n * a.n;
+    uint2 u;
+    __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&u);
+    hp[0] = __halves2bfloat162(h[0], h[1]);
+    hp[1] = __halves2bfloat162(h[2], h[3]);
+    *reinterpret_cast<uint2*>(o + static_cast<int64_t>(row) * a.n + col) = u;
+    if (sc > sr) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[static_cast<int64_t>(col + e) * a.n + row] = h[e];
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1300,6 +1378,15 @@ bool map_square(OperandMaps* o, const __nv_bfloat16* hi, const __nv_bfloat16* lo
 
 bool ns_final_fused(int iters, bool x3) { return !x3 && iters > kLoIters; }
 
+int gram_ksplit(int n_pad, int m_pad, bool x3) {
+  // single-tile Grams (n <= 128) over a long K: up to 8 slices of >= 16 k-blocks
+  if (x3 || n_pad != kBM) return 1;
+  const int nkb = m_pad / kBK;
+  int sl = 1;
+  while (sl * 2 <= 8 && nkb / (sl * 2) >= 16 && nkb % (sl * 2) == 0) sl *= 2;
+  return sl;
+}
+
 bool ns_final_has_lo(int iters, bool x3) { return x3 || iters < kLoIters; }
 
 cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
@@ -1371,10 +1458,51 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.mscale = first ? a.inv_s : nullptr;
     g.status = a.status; g.timeout_ns = a.timeout_ns;
     g.reverse = (launch++ & 1) == 0;
-    const OperandMaps& gram_out = (cc != 0.f) ? S : P;
-    e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], gram_out, g, f_gram, st)
-           : launch_sym<kEpiGram>(bn_sq, pair, X[cur], gram_out, g, f_gram, st);
-    if (e != cudaSuccess) return e;
+    const int ksplit = (a.partial != nullptr && !pair) ? gram_ksplit(n, m, x3) : 1;
+    if (ksplit > 1) {
+      // split-K: raw slice sums into the partial buffer, then k_gram_reduce
+      GemmParams gs = g;
+      gs.ksplit = ksplit;
+      gs.partial = a.partial;
+      gs.total_tiles = g.total_tiles * ksplit;
+      gs.reverse = 0;
+      e = launch_sym<kEpiGram>(bn_sq, pair, X[cur], (cc != 0.f) ? S : P, gs, f_gram, st);
+      if (e != cudaSuccess) return e;
+      GramReduceArgs ra{};
+      ra.partial = a.partial;
+      ra.ksplit = ksplit;
+      ra.batch = batch;
+      ra.n = n;
+      ra.bn = bn_sq;
+      ra.out = g.out;
+      ra.cb = g.cb;
+      ra.cd = g.cd;
+      ra.mscale = g.mscale;
+      ra.pdiag = g.pdiag;
+      cudaLaunchConfig_t rc = {};
+      cudaLaunchAttribute rattr[1];
+      rc.blockDim = dim3(256);
+      const int64_t work = static_cast<int64_t>(batch) * n * (n / 4);
+      rc.gridDim = dim3(static_cast<unsigned>(
+          std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8 * sm_count()))));
+      rc.stream = st;
+      if (kUsePdl) {
+        rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        rattr[0].val.programmaticStreamSerializationAllowed = 1;
+        rc.attrs = rattr;
+        rc.numAttrs = 1;
+      }
+      prof_begin(kKindGram, st);
+      e = cudaLaunchKernelEx(&rc, k_gram_reduce, ra);
+      prof_end(kKindGram, st, 0.0, 0.0);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    } else {
+      const OperandMaps& gram_out = (cc != 0.f) ? S : P;
+      e = x3 ? launch_sym<kEpiGram | kEpiX3>(bn_sq, pair, X[cur], gram_out, g, f_gram, st)
+             : launch_sym<kEpiGram>(bn_sq, pair, X[cur], gram_out, g, f_gram, st);
+      if (e != cudaSuccess) return e;
+    }
 
     if (cc != 0.f) {
       GemmParams q = g;

@@ -138,6 +138,43 @@ def test_ns_batched_equals_unbatched_bitwise():
         assert torch.equal(one[0], whole[b])
 
 
+# Grams of at most 128 rows over a long K are split into K-slices summed by a
+# separate pass (2 slices at K = 2048, 4 at K >= 4096).
+SPLIT_SHAPES = [(128, 2048), (96, 4096), (4096, 120), (128, 8192)]
+
+
+@pytest.mark.parametrize("rows,cols", SPLIT_SHAPES)
+def test_ns_split_k_gram_matches_oracle(rows, cols):
+    rng = np.random.default_rng(rows + cols)
+    x = torch.tensor(rng.standard_normal((3, rows, cols)), dtype=torch.bfloat16).to(DEV)
+    got = run_ns(x)
+    want = oracle_ns_batch(x)
+    for b in range(3):
+        assert rel_fro(f64(got[b]), want[b]) <= NS_TOL, b
+
+
+@pytest.mark.parametrize("name", ["gram", "square", "mixed"])
+def test_ns_split_k_single_stage_schedules(name):
+    """The split Gram's epilogue pass: 1/||X||^2 scale, and with c = 0 the
+    (a - 1) shift and P's diagonal residual written by that pass."""
+    stages = ISOLATING_SCHEDULES[name]
+    rng = np.random.default_rng(11)
+    x = torch.tensor(rng.standard_normal((2, 128, 4096)), dtype=torch.bfloat16).to(DEV)
+    got = run_ns(x, m.Schedule(stages))
+    want = oracle_ns_batch(x, stages)
+    for b in range(2):
+        assert rel_fro(f64(got[b]), want[b]) <= NS_TOL
+
+
+def test_ns_split_k_batched_equals_unbatched_bitwise():
+    rng = np.random.default_rng(17)
+    x = torch.tensor(rng.standard_normal((6, 128, 4096)), dtype=torch.bfloat16).to(DEV)
+    whole = run_ns(x)
+    for b in (0, 3, 5):
+        one = run_ns(x[b:b + 1].clone())
+        assert torch.equal(one[0], whole[b])
+
+
 # ---------------------------------------------------------------------------
 # the full step
 # ---------------------------------------------------------------------------
@@ -202,6 +239,35 @@ def test_stacked_bf16_steps_and_ragged_shapes():
                 ref = oracle.muon_step(W0[b], G0[b], M0[b], hp)
                 assert np.max(ulp_diff_f32(M[b].cpu().numpy(), momentum_ref_f32(M0[b], G0[b], hp))) <= 1
                 check_w(f64(W[b]), ref["W"], hp, ref["scale"], bf16=True)
+
+
+@pytest.mark.parametrize("offset", [0, 8])
+def test_w_rows_not_32_byte_aligned(offset):
+    """W, G and M as views with a padded row stride (520 elements: bf16 rows
+    alternate between 32- and 16-byte alignment) and, with offset 8, a base
+    16 bytes past a 32-byte boundary: the last update's W read-modify-write
+    takes its 16-byte path and must give the same result as the oracle."""
+    W0, G0, M0 = workloads.random_case(44, 256, 512, batch=2)
+    pad = 520
+
+    def padded(t):
+        big = torch.zeros(t.shape[0], t.shape[1], pad + offset, dtype=t.dtype, device=DEV)
+        v = big[:, :, offset:offset + t.shape[2]]
+        v.copy_(t.to(DEV))
+        return big, v
+
+    (Wb, W), (Gb, G), (Mb, M) = padded(W0), padded(G0), padded(M0)
+    assert (W.data_ptr() % 32 == 0) == (offset == 0) and W.stride(2) == 1
+    group = m.Group([W[0], W[1]], [G[0], G[1]], [M[0], M[1]])
+    hp = hyper()
+    code, flags = step_once([group], {})
+    assert code == m.MUON_OK and flags == 0
+    for b in range(2):
+        ref = oracle.muon_step(f64(W0[b]), f64(G0[b]), f64(M0[b]), hp)
+        check_w(f64(W[b]), ref["W"], hp, ref["scale"], bf16=True)
+        # the padding around each row is untouched
+        assert float(Wb[b, :, :offset].abs().sum()) == 0.0
+        assert float(Wb[b, :, offset + 512:].abs().sum()) == 0.0
 
 
 def test_weight_decay_mask():
