@@ -16,20 +16,26 @@
 // Frobenius normalisation is folded into the first iteration: with
 // s = ||X||_F, S_0 = (X X^T)/s^2 and X_1 = (X + P_0 X)/s.
 //
-// Kernel shapes (one persistent CTA per SM, 6 warps).  Where tile rows come
-// in pairs and BN = 256, k_ns_gemm2 runs each 256 x 256 tile on a CTA pair
-// with pair-wide tcgen05 MMAs (cta_group::2); otherwise k_ns_gemm runs
-// 128 x BN tiles per CTA (in multicast pairs when tile rows pair up).
+// Kernel shapes (one persistent CTA per SM).  Where tile rows come in pairs
+// and BN = 256, k_ns_gemm2 runs each 256 x 256 tile on a CTA pair with
+// pair-wide tcgen05 MMAs (cta_group::2, 10 warps); otherwise k_ns_gemm runs
+// 128 x BN tiles per CTA (6 warps; in multicast pairs when tile rows pair
+// up), and a Gram of a single 128 x 128 tile over a long K is split into
+// K-slices whose fp32 sums k_gram_reduce adds in a fixed order.
 // Roles:
 //   warp 0      one thread issues TMA loads of A and B k-blocks into a
 //               multi-stage shared-memory ring (128-byte swizzle);
 //   warp 1      allocates TMEM and one thread issues tcgen05.mma
-//               (M=128, N=BN, K=16, bf16 -> fp32) into one of two TMEM
-//               accumulators, committing to mbarriers;
-//   warps 2-5   epilogue (one per 32-lane TMEM quarter): tcgen05.ld, fp32
-//               epilogue math, bf16 stores (and the mirrored store of
-//               off-diagonal symmetric tiles).
+//               (bf16 -> fp32) into one of two TMEM accumulators,
+//               committing to mbarriers;
+//   the rest    epilogue (4 warps, or 8 in k_ns_gemm2: two per 32-lane TMEM
+//               quarter): tcgen05.ld, fp32 epilogue math, 256-bit residual
+//               loads, and bf16 stores -- in k_ns_gemm2 through per-warp
+//               staging boxes and TMA stores, the transposed copy of
+//               off-diagonal symmetric tiles included.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Consecutive launches walk the batch in opposite directions, so that each
+// starts on the matrices its predecessor wrote last.
 //
 // Precision.  Operands are bf16 with fp32 accumulation; S and P are stored
 // as bf16; the iterate is stored as two bf16 planes X = hi + lo with
