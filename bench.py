@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--prof-steps", type=int, default=50)
+    ap.add_argument("--layers", type=int, default=32,
+                    help="dense: layers of the matrix set (fewer: a small case, e.g. for ncu)")
+    ap.add_argument("--experts", type=int, default=256,
+                    help="moe: experts of the set (fewer: a small case, e.g. for ncu)")
     ap.add_argument("--merge", type=int, choices=[0, 1], default=0,
                     help="dense / moe: groups of one wide shape share a Newton–Schulz chain")
     ap.add_argument("--prec", choices=["bf16", "x3"], default="bf16",
@@ -86,19 +90,20 @@ def build_workload(name: str, rank: int):
                           m_dtype="fp32", scale="spectral", seed=2))
 
 
-def device_sets(name: str, rank: int, dev):
+def device_sets(name: str, rank: int, dev, layers: int = 32, experts: int = 256):
     """Multi-GB sets drawn on the device: {shape name: (W [B,r,c], G, M)}."""
     import workloads
     if name == "dense":
-        sets = workloads.dense_layers(seed=3 + 1000 * rank, device=dev)
-        desc = dict(workload="dense: 32 layers x {q,o 4096^2; k,v 1024x4096; gate,up 14336x4096; "
-                             "down 4096x14336}", matrices=32 * 7, w_dtype="bf16", g_dtype="bf16",
-                    m_dtype="fp32", scale="spectral", seed=3, grads="Gaussian 1e-3 + rank-8 spike")
+        sets = workloads.dense_layers(seed=3 + 1000 * rank, layers=layers, device=dev)
+        desc = dict(workload=f"dense: {layers} layers x {{q,o 4096^2; k,v 1024x4096; gate,up "
+                             f"14336x4096; down 4096x14336}}", matrices=layers * 7,
+                    w_dtype="bf16", g_dtype="bf16", m_dtype="fp32", scale="spectral", seed=3,
+                    grads="Gaussian 1e-3 + rank-8 spike")
     else:
-        sets = workloads.moe_experts(seed=4 + 1000 * rank, device=dev)
-        desc = dict(workload="moe: 256 experts x {up 2048x7168, down 7168x2048}", matrices=512,
-                    w_dtype="bf16", g_dtype="bf16", m_dtype="fp32", scale="spectral", seed=4,
-                    grads="1e-3 * Student-t(3)")
+        sets = workloads.moe_experts(seed=4 + 1000 * rank, experts=experts, device=dev)
+        desc = dict(workload=f"moe: {experts} experts x {{up 2048x7168, down 7168x2048}}",
+                    matrices=2 * experts, w_dtype="bf16", g_dtype="bf16", m_dtype="fp32",
+                    scale="spectral", seed=4, grads="1e-3 * Student-t(3)")
     return sets, desc
 
 
@@ -328,7 +333,7 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     if args.workload in ("dense", "moe"):
-        sets, desc = device_sets(args.workload, rank, dev)
+        sets, desc = device_sets(args.workload, rank, dev, args.layers, args.experts)
         groups = [set_groups(m, sets)]
         P = int(sum(W.numel() for W, _, _ in sets.values()))
         wl = {"kind": args.workload, "sets": sets, "desc": desc}
@@ -518,8 +523,8 @@ def run_ours(args):
     desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
                 l2={"stack": "inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M "
                              "+ 768 MiB workspace",
-                    "dense": "inputs larger than L2 (about 56 GB of W, G, M)",
-                    "moe": "inputs larger than L2 (about 60 GB of W, G, M)"}.get(
+                    "dense": f"inputs larger than L2 (about {P * 8 / 1e9:.0f} GB of W, G, M)",
+                    "moe": f"inputs larger than L2 (about {P * 8 / 1e9:.0f} GB of W, G, M)"}.get(
                     wl["kind"], "small workload (L2-resident between steps)"))
     out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,

@@ -98,6 +98,7 @@ constexpr bool kUsePdl = MUON_PDL != 0;
 #endif
 constexpr bool kUseTwoSm = MUON_TWO_SM != 0;  // pair-wide MMA (k_ns_gemm2) where BN = 256
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int kBandTiles = 8;  // update (non-symmetric, paired) tiles: column band width
 constexpr int kEpiWarps = 4;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue warps
 
@@ -190,8 +191,17 @@ __device__ __forceinline__ void decode_unit(const GemmParams& p, int t, uint32_t
   int pm = 0;
   tn = 0;
   if (!SYM) {
-    pm = l / p.tiles_n;
-    tn = l - pm * p.tiles_n;
+    // Column bands of kBandTiles tile columns, tile rows inside a band: the
+    // band's B columns (n x 2048 of X) and A (P, n x n) stay in L2 while
+    // every tile row of the band reads them.  (Row-major over all tiles
+    // streamed a 4096 x 14336 X once per tile row: 5x its size from DRAM.)
+    const int rows = p.tiles_m >> 1;
+    const int full = rows * kBandTiles;
+    const int band = l / full;
+    const int in = l - band * full;
+    const int width = min(kBandTiles, p.tiles_n - band * kBandTiles);
+    pm = in / width;
+    tn = band * kBandTiles + (in - pm * width);
   } else {
     const int S = p.tiles_n;
     for (int sr = 0; sr < S; ++sr) {
