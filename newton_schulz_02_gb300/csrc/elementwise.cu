@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kThreads) k_prepare_tall(PrepareArgs p) {
 __global__ void k_finalize_norm(FinalizeArgs p) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.batch) return;
+  if (p.gp_ctr != nullptr) p.gp_ctr[b] = 0;
   int seg = 0;
   while (seg + 1 < p.nseg && b >= p.seg_begin[seg + 1]) ++seg;
   const int parts = p.seg_parts[seg];

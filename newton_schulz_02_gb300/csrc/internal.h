@@ -73,6 +73,7 @@ struct FinalizeArgs {
   float* inv_s;  // [batch]: 1/||X||_F (0 for a zero or skipped matrix); 1 if !normalize
   int normalize;
   uint32_t* status;
+  int* gp_ctr;  // [batch] Gram arrival counters of the fused Gram + polynomial launches, zeroed here
 };
 
 // Last pass: W <- W*decay - lr_scale*O'  (mode 0), or out <- O' (mode 1).
@@ -136,6 +137,8 @@ struct NsChainArgs {
   int64_t sq_lo_off;
   FinalStore fin;       // fused into the last iteration when fin.mode != 0
   float* partial;       // split-K Gram slices, gram_ksplit(...) * batch * n_pad^2 fp32, or nullptr
+  int* gp_ctr;          // [batch] counters for the fused Gram + polynomial launches (zero on
+                        // entry), or nullptr
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -150,6 +153,7 @@ enum KernelKind : int {
   kKindApply,
   kKindTimeoutCheck,
   kKindAdamW,
+  kKindGramPoly,
   kKindCount
 };
 void prof_begin(KernelKind k, cudaStream_t st);

@@ -47,6 +47,7 @@ struct Layout {
   int64_t sq_lo_off = 0;  // split-bf16: from S's (P's) hi plane to its lo plane
   size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
   size_t kslices = 0;     // split-K Gram slices (fp32), when gram_ksplit(...) > 1
+  size_t gp_ctr = 0;      // [batch] int: Gram arrivals of the fused Gram + polynomial launches
   int ksplit = 1;
 };
 
@@ -76,6 +77,7 @@ Layout layout_for(int batch, int n_pad, int m_pad, int parts, bool x3) {
   L.partials = off; off += align256(static_cast<size_t>(batch) * L.parts * 4);
   L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
   L.skip = off; off += align256(static_cast<size_t>(batch));
+  L.gp_ctr = off; off += align256(static_cast<size_t>(batch) * 4);
   L.ksplit = gram_ksplit(n_pad, m_pad, x3);
   if (L.ksplit > 1) {
     L.kslices = off;
@@ -212,6 +214,7 @@ muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
   fa.inv_s = reinterpret_cast<float*>(ws + L.inv_s);
   fa.normalize = normalize;
   fa.status = status;
+  fa.gp_ctr = reinterpret_cast<int*>(ws + L.gp_ctr);
   cudaError_t e = launch_finalize(fa, st);
   if (e != cudaSuccess) return MUON_ERR_CUDA;
 
@@ -236,6 +239,7 @@ muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
   na.x3 = x3 ? 1 : 0;
   na.sq_lo_off = L.sq_lo_off;
   na.partial = L.ksplit > 1 ? reinterpret_cast<float*>(ws + L.kslices) : nullptr;
+  na.gp_ctr = reinterpret_cast<int*>(ws + L.gp_ctr);
   const bool fused = ns_final_fused(iters, x3);
   if (fused) {
     // the last update's epilogue writes W (or the output) from its fp32 result

@@ -97,6 +97,11 @@ constexpr bool kUsePdl = MUON_PDL != 0;
 #define MUON_TWO_SM 1
 #endif
 constexpr bool kUseTwoSm = MUON_TWO_SM != 0;  // pair-wide MMA (k_ns_gemm2) where BN = 256
+#ifndef MUON_FUSE_GRAM_POLY
+#define MUON_FUSE_GRAM_POLY 1
+#endif
+// Gram and polynomial of an iteration in one launch (k_ns_gram_poly) where possible.
+constexpr bool kFuseGramPoly = MUON_FUSE_GRAM_POLY != 0;
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kBandTiles = 8;  // update (non-symmetric, paired) tiles: column band width
 constexpr int kEpiWarps = 4;
@@ -233,8 +238,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // 32 bf16 of one row (64 bytes, 64-byte aligned in the workspace) as two
 // full-sector loads.
 __device__ __forceinline__ void load_raw4(const __nv_bfloat16* src, uint4 (&u)[4]) {
-  ld_global_v8(src, u[0], u[1]);
-  ld_global_v8(src + 16, u[2], u[3]);
+  // from L2: in a fused Gram + polynomial launch another CTA wrote these lines
+  ld_global_cg_v8(src, u[0], u[1]);
+  ld_global_cg_v8(src + 16, u[2], u[3]);
 }
 
 __device__ __forceinline__ void unpack_raw4(const uint4 (&u)[4], float (&v)[32]) {
@@ -1180,6 +1186,255 @@ __global__ void __launch_bounds__(256) k_gram_reduce(const GramReduceArgs a) {
   }
 }
 
+// Gram and polynomial of one iteration in one launch of the pair-wide
+// kernel (bf16 precision, c != 0): each CTA pair takes its Gram units, then
+// its polynomial units, with one pipeline state across both, so that its
+// producer loads polynomial operands while the epilogues drain the last Gram
+// tiles and the Gram's partly filled last round of tiles costs nothing.  A
+// polynomial unit of matrix b reads S_b, written by all of b's Gram units:
+// every epilogue warp adds 1 to the matrix's arrival counter once its TMA
+// stores of a Gram unit are complete (counted at the start of its next unit,
+// before that unit's accumulator wait, never after it), and the polynomial's
+// producer and epilogue wait (bounded) until the counter reaches the launch's
+// target.  Both phases walk the batch forward, so the first polynomial units
+// read matrices whose Gram finished about a round of tiles per matrix
+// earlier; the counters are cumulative over a call's launches (zeroed by
+// k_finalize_norm).
+constexpr int kArrivalsPerUnit = 2 * kEpiWarps2;  // epilogue warps of a CTA pair
+
+struct GramPolyParams {
+  GemmParams g;   // Gram phase
+  GemmParams q;   // polynomial phase
+  int* ctr;       // [batch] Gram arrivals, cumulative over the call's launches
+  int target;     // counter value at which this launch's Gram of a matrix is complete
+};
+
+__global__ void __launch_bounds__(kGemmThreads2, 1)
+    k_ns_gram_poly(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+                   const __grid_constant__ CUtensorMap tmSo,
+                   const __grid_constant__ CUtensorMap tmPo,
+                   const __grid_constant__ GramPolyParams P) {
+  constexpr int BN = 256;
+  constexpr uint32_t kTmemCols = kAccBufs2 * BN;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, false);
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages2 * kHalfBytes2;
+  uint8_t* staging = smem + kStages2 * kStageBytes2;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + staging_bytes2(kEpiPoly));
+  uint64_t* empty = full + kStages2;
+  uint64_t* tfull = empty + kStages2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
+  const int unit0 = static_cast<int>(blockIdx.x >> 1);
+  const int ustep = static_cast<int>(gridDim.x >> 1);
+  uint32_t* const status = P.g.status;
+  const uint64_t timeout_ns = P.g.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < kAccBufs2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * kEpiWarps2);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmS);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  griddep_wait();  // the previous kernel's outputs are this kernel's inputs
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint32_t full0 = mapa_shared(&full[0], 0);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_par = 0;
+      bool ok = true;
+      for (int ph = 0; ok && ph < 2; ++ph) {
+        const GemmParams& p = ph ? P.q : P.g;
+        const CUtensorMap* tm_ab = ph ? &tmS : &tmX;
+        const int nkb = p.K / kBK;
+        for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
+          int b, tm, tn;
+          decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
+          if (ph) {
+            // S_b complete (normally long since)
+            if (!wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_global();  // the TMA loads below read what the acquire saw
+          }
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status, timeout_ns)) {
+              ok = false;
+              break;
+            }
+            const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes2);
+            tma_load_3d_pair(smA + stage * kHalfBytes2, tm_ab, bar, kb * kBK, tm * kBM, b);
+            tma_load_3d_pair(smB + stage * kHalfBytes2, tm_ab, bar, kb * kBK,
+                             tn * BN + static_cast<int>(rank) * 128, b);
+            issued |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages2) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (leader)
+        for (int s = 0; s < kStages2; ++s)
+          if ((issued >> s) & 1u)
+            mbar_wait_drain(&full[s], (last_par >> s) & 1u, status, timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int ph = 0; ok && ph < 2; ++ph) {
+        const GemmParams& p = ph ? P.q : P.g;
+        const int nkb = p.K / kBK;
+        for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
+          if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status, timeout_ns))
+            break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, status, timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smA + stage * kHalfBytes2);
+            const uint32_t b_addr = smem_u32(smB + stage * kHalfBytes2);
+#pragma unroll
+            for (int ks = 0; ks < kBK / 16; ++ks) {
+              const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+              tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair_multicast(&empty[stage], 0x3);
+            if (++stage == kStages2) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair_multicast(&tfull[acc], 0x3);
+          if (++acc == kAccBufs2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      tc_commit_pair_multicast(drain, 0x1);
+      mbar_wait_drain(drain, 0, status, timeout_ns);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    constexpr int kChunks = (BN / 32) / (kEpiWarps2 / 4);
+    const int c_begin = ((warp - 2) >> 2) * kChunks;
+    const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
+    uint8_t* sbuf = staging + (warp - 2) * kStagingPerWarp2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int pending = -1;  // matrix of the last Gram unit whose arrival is not yet counted
+    bool ok = true;
+    for (int ph = 0; ok && ph < 2; ++ph) {
+      const GemmParams& p = ph ? P.q : P.g;
+      for (int t = unit0; t < p.total_tiles; t += ustep) {
+        if (pending >= 0) {
+          if (lane == 0) {
+            tma_store_wait_all0();
+            fence_proxy_async_global();
+            red_release_gpu_add(P.ctr + pending, 1);
+          }
+          pending = -1;
+        }
+        int b, tm, tn;
+        decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
+        bool r;
+        if (ph == 0) {
+          r = epilogue_tile<BN, kEpiGram, true, kChunks, true>(
+              p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
+              acc_phase, abort_flag, c_begin, &tmSo, &tmSo, sbuf);
+        } else {
+          // the epilogue reads S_b itself (b S term): wait for it here too
+          int ready = 1;
+          if (lane == 0)
+            ready = wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns);
+          ready = __shfl_sync(0xffffffffu, ready, 0);
+          if (!ready) {
+            ok = false;
+            break;
+          }
+          r = epilogue_tile<BN, kEpiPoly, true, kChunks, true>(
+              p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
+              acc_phase, abort_flag, c_begin, &tmPo, &tmPo, sbuf);
+        }
+        if (!r) {
+          ok = false;
+          break;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+        if (++acc == kAccBufs2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        if (ph == 0) pending = b;
+      }
+    }
+    if (lane == 0) {
+      tma_store_wait_all0();
+      if (pending >= 0) {
+        fence_proxy_async_global();
+        red_release_gpu_add(P.ctr + pending, 1);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1336,6 +1591,46 @@ cudaError_t launch_gemm2(const CUtensorMap& ta, const CUtensorMap& ta2, const CU
 }
 
 
+// Gram + polynomial of one iteration as one launch (k_ns_gram_poly).
+cudaError_t launch_gram_poly(const CUtensorMap& x, const CUtensorMap& sk, const CUtensorMap& so,
+                             const CUtensorMap& po, const GramPolyParams& gp, double flops,
+                             cudaStream_t st) {
+  auto kern = k_ns_gram_poly;
+  constexpr size_t kSmem = smem_bytes2(kEpiPoly);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kGemmThreads2);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cfg.gridDim = dim3(2);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  // every cluster resident at once: polynomial units wait on other clusters' Gram units
+  const int units = std::max(1, std::min(gp.g.total_tiles, clusters));
+  cfg.gridDim = dim3(2 * units);
+  if (kUsePdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  prof_begin(kKindGramPoly, st);
+  e = cudaLaunchKernelEx(&cfg, kern, x, sk, so, po, gp);
+  prof_end(kKindGramPoly, st, flops, 0.0);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Tensor maps of one operand: K-major with 128-row boxes (A, and the B half a
 // CTA of a pair loads) and BN-row boxes (unpaired B), MN-major (the update's
 // B), each for the hi and the lo plane.  Operands without a lo plane carry
@@ -1446,6 +1741,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   // starts on the matrices its predecessor wrote last (still in L2); the
   // first Gram follows the prepare pass, which writes the batch in order.
   int launch = 0;
+  int gp_launches = 0;  // fused Gram + polynomial launches so far (counter targets)
   for (int it = 0; it < a.iters; ++it) {
     const float ca = a.coeffs[3 * it], cb = a.coeffs[3 * it + 1], cc = a.coeffs[3 * it + 2];
     const int cur = it & 1;
@@ -1475,7 +1771,30 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     g.status = a.status; g.timeout_ns = a.timeout_ns;
     g.reverse = (launch++ & 1) == 0;
     const int ksplit = (a.partial != nullptr && !pair) ? gram_ksplit(n, m, x3) : 1;
-    if (ksplit > 1) {
+    // polynomial parameters (c != 0)
+    GemmParams q = g;
+    q.K = n;
+    q.out = a.B;
+    q.aux = a.A; q.aux_ld = n; q.aux_bstride = static_cast<int64_t>(n) * n;
+    q.cb = cb; q.cc = cc; q.cd = x3 ? 0.f : ca - 1.f;
+    q.pdiag = x3 ? nullptr : a.pdiag;
+    q.mscale = nullptr;
+    if (x3) q.lo_in = 1;
+    // Gram and polynomial in one launch where both run on CTA pairs (bf16)
+    const bool gp_fuse = kFuseGramPoly && !x3 && pair && kUseTwoSm && bn_sq == 256 &&
+                         cc != 0.f && a.gp_ctr != nullptr && ksplit == 1;
+    if (gp_fuse) {
+      GramPolyParams gp{};
+      gp.g = g;
+      gp.q = q;
+      gp.g.reverse = 0;  // both phases walk forward (the polynomial trails the Gram)
+      gp.q.reverse = 0;
+      gp.ctr = a.gp_ctr;
+      gp.target = (++gp_launches) * g.tiles_per_matrix * kArrivalsPerUnit;
+      e = launch_gram_poly(X[cur].k128, S.k128, S.st, P.st, gp, f_gram + f_poly, st);
+      if (e != cudaSuccess) return e;
+      launch = 0;  // the update walks backwards, from the matrices the polynomial ended on
+    } else if (ksplit > 1) {
       // split-K: raw slice sums into the partial buffer, then k_gram_reduce
       GemmParams gs = g;
       gs.ksplit = ksplit;
@@ -1520,16 +1839,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
     }
 
-    if (cc != 0.f) {
-      GemmParams q = g;
-      q.K = n;
-      q.out = a.B;
-      q.aux = a.A; q.aux_ld = n; q.aux_bstride = static_cast<int64_t>(n) * n;
-      q.cb = cb; q.cc = cc; q.cd = x3 ? 0.f : ca - 1.f;
-      q.pdiag = x3 ? nullptr : a.pdiag;
-      q.mscale = nullptr;
+    if (cc != 0.f && !gp_fuse) {
       q.reverse = (launch++ & 1) == 0;
-      if (x3) q.lo_in = 1;
       e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, P, q, f_poly, st)
              : launch_sym<kEpiPoly>(bn_sq, pair, S, P, q, f_poly, st);
       if (e != cudaSuccess) return e;

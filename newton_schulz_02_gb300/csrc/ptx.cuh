@@ -84,6 +84,45 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
+// cross-CTA hand-over through global counters (two dependent GEMM phases in
+// one launch)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy accesses of global memory with its
+// async-proxy ones (TMA loads after an acquire; TMA stores before a release).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait (bounded) until *ctr >= target, with acquire semantics.  On timeout:
+// sets the abort flag and MUON_FLAG_TIMEOUT, returns false.
+__device__ __forceinline__ bool wait_counter_bounded(const int* ctr, int target,
+                                                     volatile int* abort, uint32_t* status,
+                                                     uint64_t timeout_ns) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicOr(status, 0x2u /* MUON_FLAG_TIMEOUT */);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) — 3-D tiled loads into shared memory
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -343,6 +382,15 @@ __device__ __forceinline__ void ld_global_v8(const void* p, uint4& a, uint4& b) 
                : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
                  "=r"(b.w)
                : "l"(p));
+}
+
+// Same, from L2 (bypassing L1): data another CTA of the running grid wrote.
+__device__ __forceinline__ void ld_global_cg_v8(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(p)
+               : "memory");
 }
 
 __device__ __forceinline__ void st_global_v8(void* p, const uint4& a, const uint4& b) {
