@@ -1398,6 +1398,7 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
             ok = false;
             break;
           }
+          __syncwarp();  // lane 0's acquire orders every lane's reads of S_b
           r = epilogue_tile<BN, kEpiPoly, true, kChunks, true>(
               p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
               acc_phase, abort_flag, c_begin, &tmPo, &tmPo, sbuf);
@@ -1705,7 +1706,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   if (encode_fn() == nullptr) return cudaErrorNotSupported;
   const int n = a.n_pad, m = a.m_pad, batch = a.batch;
   const int bn_sq = (n % 256 == 0) ? 256 : 128;
-  const int bn_up = (m % 256 == 0) ? 256 : 128;
+  // update tile width: 256 where the tile rows pair up (pair-wide kernel);
+  // otherwise 128, twice the tiles for a short-K, epilogue-bound update
+  const int bn_up = (m % 256 == 0 && n % 256 == 0) ? 256 : 128;
   const bool x3 = a.x3 != 0;
 
   OperandMaps X[2], S, P;
