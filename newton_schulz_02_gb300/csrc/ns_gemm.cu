@@ -34,8 +34,11 @@
 //               staging boxes and TMA stores, the transposed copy of
 //               off-diagonal symmetric tiles included.
 // The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
-// Consecutive launches walk the batch in opposite directions, so that each
-// starts on the matrices its predecessor wrote last.
+// In the bf16 precision, where tile rows pair up, k_ns_gram_poly runs an
+// iteration's Gram and polynomial as one launch (per-matrix hand-over through
+// arrival counters) and k_ns_gemm2 the update.  Consecutive launches walk the
+// batch in opposite directions, so that each starts on the matrices its
+// predecessor wrote last; the update's tiles go in column bands.
 //
 // Precision.  Operands are bf16 with fp32 accumulation; S and P are stored
 // as bf16; the iterate is stored as two bf16 planes X = hi + lo with
