@@ -270,6 +270,20 @@ def test_w_rows_not_32_byte_aligned(offset):
         assert float(Wb[b, :, offset + 512:].abs().sum()) == 0.0
 
 
+def test_empty_call_is_a_no_op():
+    """No groups: the call succeeds, clears the status word and touches nothing."""
+    W, G, M = workloads.random_case(45, 64, 64, batch=1)
+    Wd = W.to(DEV)
+    before = Wd.clone()
+    hp = m.hparams()
+    ws = m.workspace(m.muon_step_workspace_size([m.Group.stacked(Wd, G.to(DEV), M.to(DEV))]))
+    ws.fill_(0xFF)                                   # a stale status word
+    m.muon_step_batched([], hp, ws)
+    code, flags = m.muon_get_status(ws)
+    assert code == m.MUON_OK and flags == 0
+    assert torch.equal(Wd, before)
+
+
 def test_weight_decay_mask():
     W, G, M = workloads.random_case(40, 256, 256, batch=2, w_dtype=torch.float32)
     W0, G0, M0 = f64(W), f64(G), f64(M)

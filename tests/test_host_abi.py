@@ -219,6 +219,9 @@ def test_step_rejects_before_enqueue(lib):
     L = m.load_library()
     assert L.muon_step_batched(None, 1, ctypes.byref(hp), None, 0x100000, need, None) == \
         m.MUON_ERR_INVALID_ARG
+    # a group of no matrices is an error (an empty call passes no groups instead)
+    assert _step([_group(64, 64, batch=0)], hp, 0x100000, need) == m.MUON_ERR_INVALID_ARG
+    assert _ws_size([_group(64, 64, batch=0)])[0] == m.MUON_ERR_INVALID_ARG
 
 
 def test_adamw_rejects_before_enqueue(lib):
@@ -260,6 +263,11 @@ def test_newton_schulz_rejects_before_enqueue(lib):
     assert L.newton_schulz_batched(*args(0x200000, 0x200000, 0x100000, need)) == \
         m.MUON_ERR_INVALID_ARG                   # x and out overlap
     assert L.newton_schulz_batched(*args(None, 0x900000, 0x100000, need)) == m.MUON_ERR_INVALID_ARG
+    # batch 0 is rejected by the size query and by the call
+    assert L.newton_schulz_workspace_size(ctypes.byref(v), 0, None, ctypes.byref(nb)) == \
+        m.MUON_ERR_INVALID_ARG
+    assert L.newton_schulz_batched(0x200000, m.MUON_BF16, ctypes.byref(v), 0, 0x900000, m.MUON_F32,
+                                   None, 0x100000, need, None) == m.MUON_ERR_INVALID_ARG
 
 
 def test_timeout_setting(lib):
