@@ -147,6 +147,10 @@ def test_workspace_size_layout(lib):
     (8, 12, 12, m.MUON_ERR_UNSUPPORTED),
     (8, 8, 12, m.MUON_ERR_MISALIGNED),
     (3, 8, 8, m.MUON_OK),
+    (1 << 20, 8, 8, m.MUON_OK),                       # the largest side the library takes
+    (8, 1 << 20, 1 << 20, m.MUON_OK),
+    ((1 << 20) + 8, 8, 8, m.MUON_ERR_INVALID_ARG),    # beyond it: rejected, not truncated
+    (8, (1 << 20) + 8, (1 << 20) + 8, m.MUON_ERR_INVALID_ARG),
 ])
 def test_view_validation(lib, rows, cols, rs, want):
     code, _ = _ws_size([_group(rows, cols, rs)])
