@@ -14,7 +14,7 @@ import torch
 import newton_schulz_02_gb300 as m
 import oracle
 import workloads
-from tests.gpu_util import F32, check_w, f64, hyper, momentum_ref_f32, rel_fro, ulp_diff_f32
+from tests.gpu_util import check_w, f64, hyper, momentum_ref_f32, rel_fro, ulp_diff_f32
 
 pytestmark = pytest.mark.gpu
 
