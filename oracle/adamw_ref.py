@@ -17,7 +17,7 @@ Sources (web pages, cited by title and section):
   decay mask (biases off, norm scales configurable, embeddings and the
   output layer on, everything else on).
 
-Reading where the pages are silent (listed in the design doc): the pages name
+Reading where the pages are silent: the pages name
 AdamW without writing its update; it is taken as Adam with bias correction
 and decoupled decay (Loshchilov & Hutter), eps added outside the square
 root, which is the form optax's ``adamw`` and PyTorch's ``AdamW`` compute:

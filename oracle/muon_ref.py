@@ -30,7 +30,7 @@ Sources (web pages, cited by title and section):
 * RFC-0023 §方案 4 (muon_batch_update): same-shape matrices are stacked and
   orthogonalised in one batched call, chunked by a batch size.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * bias correction bc(x, k) = x / (1 - beta**k), with t >= 1 counting steps
   including the current one;
