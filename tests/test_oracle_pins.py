@@ -229,11 +229,15 @@ def test_p8_scale_examples():
     check_scale_golden(oracle.update_scale)
 
 
-def test_p8_weight_decay_examples():
+def check_weight_decay_golden(fn):
     for W, O, lr, wd, s, decay, want in read_golden("weight_decay_examples.txt"):
-        got = oracle.decoupled_update(np.array([[float(W)]]), np.array([[float(O)]]),
-                                      float(lr), float(wd), float(s), bool(int(decay)))
+        got = fn(np.array([[float(W)]]), np.array([[float(O)]]),
+                 float(lr), float(wd), float(s), bool(int(decay)))
         assert abs(got[0, 0] - float(want)) < 1e-15
+
+
+def test_p8_weight_decay_examples():
+    check_weight_decay_golden(oracle.decoupled_update)
 
 
 def test_full_step_composition():
@@ -398,3 +402,27 @@ def test_planted_scale_mistake_is_caught():
         return oracle.update_scale(r, c, mode, gamma, 1 - axis)
     with pytest.raises(AssertionError):
         check_scale_golden(bad_axis)
+
+
+def _wd_without_lr(W, O, lr, wd, scale, decay=True):
+    """Decay by (1 - lambda) in place of (1 - eta*lambda)."""
+    return W * ((1.0 - wd) if decay else 1.0) - lr * scale * O
+
+
+def _wd_mask_ignored(W, O, lr, wd, scale, decay=True):
+    return W * (1.0 - lr * wd) - lr * scale * O
+
+
+def _wd_sign_of_step(W, O, lr, wd, scale, decay=True):
+    return W * ((1.0 - lr * wd) if decay else 1.0) + lr * scale * O
+
+
+def _wd_coupled(W, O, lr, wd, scale, decay=True):
+    """Decay folded into the scaled step (lambda*W added to O before the scale)."""
+    return W - lr * scale * (O + (wd * W if decay else 0.0))
+
+
+@pytest.mark.parametrize("bad", [_wd_without_lr, _wd_mask_ignored, _wd_sign_of_step, _wd_coupled])
+def test_planted_weight_decay_mistakes_are_caught(bad):
+    with pytest.raises(AssertionError):
+        check_weight_decay_golden(bad)
