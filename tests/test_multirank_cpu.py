@@ -1,6 +1,7 @@
-"""The N > 1 bench path on CPU: two gloo ranks on 127.0.0.1 check the
+"""The bench's host logic on CPU: two gloo ranks on 127.0.0.1 check the
 cross-rank reduction of the timed region (max over ranks) and the whole-job
-value, and that the reference arm does no work on ranks other than 0."""
+value; the reference arm does no work on ranks other than 0, and on rank 0
+prints one contract line."""
 import os
 import socket
 
@@ -58,3 +59,27 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
         steps, warmup, gpus, workload = 2, 1, 2, "stack"
     assert bench.run_reference(A()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """Rank 0 of the reference arm times the float64 oracle on host cores and
+    prints one JSON line carrying the keys of the bench contract."""
+    import json
+
+    class A:
+        steps, warmup, gpus, workload = 2, 1, 1, "single"
+    assert bench.run_reference(A()) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "params/s" and d["value"] > 0
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 2, 1)
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["ms_per_step"] > 0 and d["dtype"] == "f64" and d["data"] == "synthetic"
+    assert d["config"]["workload"].startswith("single") and d["config"]["rows"] == 256
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert "matrices of 256x512" in cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
