@@ -183,7 +183,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = [n for k, n in enumerate(names) if any(r[5 + k].lower() == "active" for r in rows)]
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": float(rows[0][2]),
-                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()),
+                                   default=None),
                 "reasons": reasons, "samples": len(rows)}
 
 

@@ -83,3 +83,23 @@ def test_reference_arm_prints_the_contract_line(capsys):
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_clock_summary_parses_nvidia_smi_rows(tmp_path):
+    """The clocks object is read from nvidia-smi's csv rows (noheader, nounits):
+    median SM clock under load, the maximum, and every throttle reason seen."""
+    cs = bench.ClockSampler(0)
+    cs.path = str(tmp_path / "clocks.csv")
+    cs.proc = object()                       # stands for the sampler process
+    rows = ["0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1440, 2070, 1398.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1425, 2070, [N/A], 0x4, Not Active, Not Active, Not Active, Active",
+            "garbage line"]
+    open(cs.path, "w").write("\n".join(rows) + "\n")
+    d = cs.summary()
+    assert d["sm_mhz"] == 1440.0 and d["sm_max_mhz"] == 2070.0 and d["samples"] == 3
+    assert d["reasons"] == ["sw_power_cap"] and d["power_w_max"] == 1398.0
+
+    open(cs.path, "w").write("0, 1300, 2070, [N/A], 0x40, Not Active, Active, Not Active, Not Active\n")
+    d = cs.summary()
+    assert d["reasons"] == ["hw_thermal_slowdown"] and d["power_w_max"] is None
