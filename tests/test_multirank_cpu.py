@@ -103,3 +103,17 @@ def test_clock_summary_parses_nvidia_smi_rows(tmp_path):
     open(cs.path, "w").write("0, 1300, 2070, [N/A], 0x40, Not Active, Active, Not Active, Not Active\n")
     d = cs.summary()
     assert d["reasons"] == ["hw_thermal_slowdown"] and d["power_w_max"] is None
+
+
+def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path):
+    """roofline.traffic comes from a committed ncu summary only while the
+    kernel source it was taken on is unchanged; otherwise it is null."""
+    import json
+    p = tmp_path / "traffic.json"
+    entry = {"kernels": {"ns_gram_poly": {"dram_bytes_per_launch_full_workload": 123.0}}}
+    p.write_text(json.dumps(dict(entry, source_hash=bench.kernel_source_hash())))
+    assert bench.read_traffic("ns_gram_poly", summary=str(p)) == 123.0
+    assert bench.read_traffic("ns_update", summary=str(p)) is None
+    p.write_text(json.dumps(dict(entry, source_hash="0" * 16)))
+    assert bench.read_traffic("ns_gram_poly", summary=str(p)) is None
+    assert bench.read_traffic("ns_gram_poly", summary=str(tmp_path / "absent.json")) is None
