@@ -19,9 +19,9 @@
 // Kernel shapes (one persistent CTA per SM).  Where tile rows come in pairs
 // and BN = 256, k_ns_gemm2 runs each 256 x 256 tile on a CTA pair with
 // pair-wide tcgen05 MMAs (cta_group::2, 10 warps); otherwise k_ns_gemm runs
-// 128 x BN tiles per CTA (6 warps; in multicast pairs when tile rows pair
-// up), and a Gram of a single 128 x 128 tile over a long K is split into
-// K-slices whose fp32 sums k_gram_reduce adds in a fixed order.
+// 128 x BN tiles per CTA (6 warps), and a Gram of a single 128 x 128 tile
+// over a long K is split into K-slices whose fp32 sums k_gram_reduce adds in
+// a fixed order.
 // Roles:
 //   warp 0      one thread issues TMA loads of A and B k-blocks into a
 //               multi-stage shared-memory ring (128-byte swizzle);
@@ -88,7 +88,6 @@ namespace {
 constexpr int kBM = 128;  // tile rows (TMEM lanes)
 constexpr int kResidualIters = 0;  // iterations whose product also reads the lo plane
 constexpr int kLoIters = 4;        // iterations that read the lo plane (the first kLoIters-1 write it)
-constexpr bool kUsePairs = true;   // 2-CTA clusters sharing the B tile (see k_ns_gemm)
 #ifndef MUON_PDL
 #define MUON_PDL 1
 #endif
@@ -695,18 +694,13 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
   return true;
 }
 
-// PAIR: launched in clusters of two CTAs that compute vertically adjacent
-// tiles of the same tile column.  Each CTA loads its own A tile and half of
-// the shared B tile, multicasting that half into both CTAs' shared memory,
-// so each CTA fetches 32 KB instead of 48 KB per k-block from L2.  A stage is
-// refilled only after both CTAs' MMAs have consumed it (each MMA commit
-// arrives on the stage's empty barrier in both CTAs).
-template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
+// One CTA per 128 x BN tile (shapes whose tile rows do not pair up, and the
+// split-K Grams); every CTA loads its own A and B tiles.
+template <int BN, bool B_MN, int EPI, bool SYM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_ns_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
               const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
               const GemmParams p) {
-  static_assert(!(SYM && PAIR) || BN == 256, "symmetric pairs are 256-row super-rows");
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
   constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN, B_MN);
@@ -725,14 +719,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit0 = static_cast<int>(blockIdx.x);
+  const int ustep = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], PAIR ? 2 : 1);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -753,7 +746,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch_dependents();
@@ -772,7 +764,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
         int b, tm, tn;
-        decode_unit<BN, SYM, PAIR>(p, t / nsplit, rank, b, tm, tn);
+        decode_unit<BN, SYM, false>(p, t / nsplit, 0u, b, tm, tn);
         int plane = 0, kk = (t % nsplit) * nkb_run;    // operand plane, k-block within it
         for (int kb = 0; kb < nkb_run; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -788,21 +780,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           tma_load_3d(smA + stage * C::kABytes, ta, &full[stage], k0, tm * kBM, b);
-          if (PAIR) {
-            // this CTA's half of B, into both CTAs (the B map's box is half the tile)
-            if (!B_MN) {
-              tma_load_3d_multicast(smB + stage * C::kBBytes + rank * (C::kBBytes / 2), tb,
-                                    &full[stage], k0, tn * BN + static_cast<int>(rank) * (BN / 2),
-                                    b, 0x3);
-            } else {
-#pragma unroll
-              for (int j = 0; j < BN / 128; ++j) {
-                const int jj = static_cast<int>(rank) * (BN / 128) + j;
-                tma_load_3d_multicast(smB + stage * C::kBBytes + jj * (64 * kBK * 2), tb,
-                                      &full[stage], tn * BN + jj * 64, k0, b, 0x3);
-              }
-            }
-          } else if (!B_MN) {
+          if (!B_MN) {
             tma_load_3d(smB + stage * C::kBBytes, tb, &full[stage], k0, tn * BN, b);
           } else {
 #pragma unroll
@@ -857,10 +835,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_mma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          if (PAIR)
-            tc_commit_multicast(&empty[stage], 0x3);
-          else
-            tc_commit(&empty[stage]);
+          tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -882,7 +857,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = unit0; t < p.total_tiles; t += ustep) {
       int b, tm, tn;
-      decode_unit<BN, SYM, PAIR>(p, t / nsplit, rank, b, tm, tn);
+      decode_unit<BN, SYM, false>(p, t / nsplit, 0u, b, tm, tn);
       if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
                                        q, lane, &tfull[acc], acc_phase, abort_flag, 0, nullptr,
                                        nullptr, nullptr, t % nsplit))
@@ -896,7 +871,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync_all();  // no CTA leaves while its peer may still write into it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -1507,11 +1481,11 @@ bool map_store(CUtensorMap* m, const void* base, int batch, int rows, int cols) 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool B_MN, int EPI, bool SYM, bool PAIR>
+template <int BN, bool B_MN, int EPI, bool SYM>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUtensorMap& tb,
                         const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
                         cudaStream_t st) {
-  auto kern = k_ns_gemm<BN, B_MN, EPI, SYM, PAIR>;
+  auto kern = k_ns_gemm<BN, B_MN, EPI, SYM>;
   const size_t smem = Cfg<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -1519,27 +1493,13 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUt
   const KernelKind kind = epi_kind(EPI) == kEpiGram ? kKindGram
                           : (epi_kind(EPI) == kEpiPoly ? kKindPoly : kKindUpdate);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  int units_in_flight = sm_count();
-  if (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(2);
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    units_in_flight = clusters;
-  }
-  const int units = std::max(1, std::min(p.total_tiles, units_in_flight));
-  cfg.gridDim = dim3(PAIR ? 2 * units : units);
+  const int units = std::max(1, std::min(p.total_tiles, sm_count()));
+  cfg.gridDim = dim3(units);
   if (kUsePdl) {
     attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
@@ -1645,33 +1605,28 @@ struct OperandMaps {
 };
 
 // Gram / polynomial: A and B are the same symmetric operand (X or S).
+// `pair`: the pair-wide kernel (tile rows pair up and BN = 256).
 template <int EPI>
 cudaError_t launch_sym(int bn, bool pair, const OperandMaps& A, const OperandMaps& O,
                        const GemmParams& p, double f, cudaStream_t st) {
-  if (bn == 256 && pair && kUseTwoSm)
+  if (bn == 256 && pair)
     return launch_gemm2<false, EPI, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, O.st, O.st_lo, p,
                                           f, st);
-  if (bn == 256 && pair)
-    return launch_gemm<256, false, EPI, true, true>(A.k128, A.k128_lo, A.k128, A.k128_lo, p, f, st);
   if (bn == 256)
-    return launch_gemm<256, false, EPI, true, false>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
-  return launch_gemm<128, false, EPI, true, false>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
+    return launch_gemm<256, false, EPI, true>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
+  return launch_gemm<128, false, EPI, true>(A.k128, A.k128_lo, A.kbn, A.kbn_lo, p, f, st);
 }
 
 // Update: A = P (K-major), B = X (MN-major).
 template <int EPI>
 cudaError_t launch_upd(int bn, bool pair, const OperandMaps& Pm, const OperandMaps& Xm,
                        const OperandMaps& Om, const GemmParams& p, double f, cudaStream_t st) {
-  if (bn == 256 && pair && kUseTwoSm)
+  if (bn == 256 && pair)
     return launch_gemm2<true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, Om.st, Om.st_lo,
                                           p, f, st);
-  if (bn == 256 && pair)
-    return launch_gemm<256, true, EPI, false, true>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
   if (bn == 256)
-    return launch_gemm<256, true, EPI, false, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
-  if (pair)
-    return launch_gemm<128, true, EPI, false, true>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
-  return launch_gemm<128, true, EPI, false, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+    return launch_gemm<256, true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
+  return launch_gemm<128, true, EPI, false>(Pm.k128, Pm.k128_lo, Xm.mn, Xm.mn_lo, p, f, st);
 }
 
 bool map_square(OperandMaps* o, const __nv_bfloat16* hi, const __nv_bfloat16* lo, int batch, int n,
@@ -1754,8 +1709,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     const bool first = (it == 0);
     cudaError_t e;
 
-    // Pair clusters whenever the tile rows come in pairs (n_pad % 256 == 0).
-    const bool pair = kUsePairs && (n % 256 == 0);
+    // The pair-wide kernel wherever the tile rows come in pairs (n_pad % 256 == 0).
+    const bool pair = kUseTwoSm && (n % 256 == 0);
 
     GemmParams g{};
     g.M = n; g.N = n; g.K = m;
@@ -1787,7 +1742,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     q.mscale = nullptr;
     if (x3) q.lo_in = 1;
     // Gram and polynomial in one launch where both run on CTA pairs (bf16)
-    const bool gp_fuse = kFuseGramPoly && !x3 && pair && kUseTwoSm && bn_sq == 256 &&
+    const bool gp_fuse = kFuseGramPoly && !x3 && pair && bn_sq == 256 &&
                          cc != 0.f && a.gp_ctr != nullptr && ksplit == 1;
     if (gp_fuse) {
       GramPolyParams gp{};
@@ -1855,7 +1810,8 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     GemmParams u{};
     u.M = n; u.N = m; u.K = n;
     u.tiles_m = n / kBM; u.tiles_n = m / bn_up;
-    u.tiles_per_matrix = pair ? (u.tiles_m / 2) * u.tiles_n : u.tiles_m * u.tiles_n;
+    u.tiles_per_matrix = (pair && bn_up == 256) ? (u.tiles_m / 2) * u.tiles_n
+                                                : u.tiles_m * u.tiles_n;
     u.total_tiles = u.tiles_per_matrix * batch;
     u.out = xb[cur ^ 1]; u.out_ld = m; u.out_bstride = static_cast<int64_t>(n) * m;
     u.aux = xb[cur]; u.aux_ld = m; u.aux_bstride = static_cast<int64_t>(n) * m;

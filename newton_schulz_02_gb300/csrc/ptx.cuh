@@ -147,20 +147,6 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t c0,
                : "memory");
 }
 
-// Same load, multicast: the box lands at the same shared-memory offset in
-// every CTA of `cta_mask` (this GPU's own memory only) and completes bytes
-// on the mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const void* tmap,
-                                                      uint64_t* bar, int32_t c0, int32_t c1,
-                                                      int32_t c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Tiled store of a shared-memory box to global memory (bulk-group
 // completion).  The issuing thread must have ordered the box's generic-proxy
 // writes before it with fence.proxy.async (see fence_proxy_async_smem).
@@ -329,16 +315,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// Commit that arrives once on the mbarrier at the same offset in every CTA of
-// `cta_mask` when this thread's tcgen05 ops so far finish.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
