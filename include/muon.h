@@ -251,12 +251,16 @@ muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
  * returns MUON_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.  The
  * call allocates no device memory.
  *
- * The first call on a device looks up the array's device address on that
- * device (cudaGetSymbolAddress, with the device current), so make that first
- * call before any stream capture.  All calls share the one array and every
- * call rewrites what it reads, so stale contents do not matter, but calls
- * that may overlap on the GPU (different streams, several host threads)
- * race on it and must be serialised by the caller.
+ * The first call in each CUDA context looks up the array's device address
+ * in that context (cudaGetSymbolAddress, with the device current; kept for
+ * later calls in the same context, keyed by the context's unique id, so a
+ * context created after cudaDeviceReset gets a fresh lookup), so make that
+ * first call before any stream capture.  All calls share the one array: each
+ * call clears what must start at zero (status word, skip flags, hand-over
+ * counters) and rewrites everything else it reads, so the previous call's
+ * contents do not matter, but calls that may overlap on the GPU (different
+ * streams, several host threads) race on it and must be serialised by the
+ * caller.
  *
  * device_flags: NULL, or a caller-owned 4-byte-aligned device word that
  * receives this call's MUON_FLAG_* bits (stream-ordered copy at the end). */

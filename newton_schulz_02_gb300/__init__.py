@@ -338,7 +338,14 @@ def newton_schulz_batched_noalloc(x: torch.Tensor, out: torch.Tensor, schedule=N
     if x3.stride(2) != 1 or not out.is_contiguous():
         raise ValueError("x needs unit column stride and out must be contiguous")
     view = muon_view_t(x3.shape[1], x3.shape[2], x3.stride(1), x3.stride(0), 0)
-    flags_ptr = device_flags.data_ptr() if device_flags is not None else None
+    flags_ptr = None
+    if device_flags is not None:
+        # one 4-byte word on the device x lives on: the call ends with a
+        # device-to-device copy of its status word into it
+        if not (device_flags.is_cuda and device_flags.device == x.device
+                and device_flags.element_size() == 4 and device_flags.numel() >= 1):
+            raise ValueError("device_flags must be a non-empty 4-byte tensor on x's device")
+        flags_ptr = device_flags.data_ptr()
     return load_library().newton_schulz_batched_noalloc(
         x.data_ptr(), _DT[x.dtype], ctypes.byref(view), x3.shape[0], out.data_ptr(),
         _DT[out.dtype], _sched_ref(schedule), flags_ptr, _stream(stream))

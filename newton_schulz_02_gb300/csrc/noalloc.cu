@@ -12,8 +12,12 @@
 // The array is part of the library's device image: every GPU the library is
 // loaded on holds its kStaticScratchBytes until the process exits.  Host code
 // cannot use the array's name as a device address; its device address is
-// taken once per device with cudaGetSymbolAddress (with that device current)
-// on the first call made on that device.
+// looked up with cudaGetSymbolAddress (with the device current) on the first
+// call made in a CUDA context, and kept for later calls in that context.
+// The cache is keyed by the context's process-unique id (cuCtxGetId), so an
+// address taken in one context is never handed to kernels of another, not
+// even of a context created after cudaDeviceReset under a reused handle.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,23 +32,73 @@ constexpr int kMaxDevices = 128;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // context the address was taken in
+  void* ptr = nullptr;
+};
 
-// Device address of g_static_scratch on the current device (set up once per device).
+std::mutex g_scratch_mu;
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver entry points, through the runtime's query (the library links no
+// driver stub).
+void* driver_fn(const char* name, int version) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return f;
+}
+
+// Process-unique id of the current context; 0 if no context is current.
+cudaError_t current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = reinterpret_cast<CtxGetCurrentFn>(driver_fn("cuCtxGetCurrent", 4000));
+    get_id = reinterpret_cast<CtxGetIdFn>(driver_fn("cuCtxGetId", 12000));
+  });
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorDeviceUninitialized;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// Device address of g_static_scratch in the current device's current context.
 cudaError_t static_scratch(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (id != 0 && a.ptr != nullptr && a.ctx_id == id) {
+    *out = a.ptr;
+    return cudaSuccess;
   }
-  *out = g_scratch_addr[dev];
+  // First call in this context (with no context current yet, the lookup
+  // makes the device's primary context current).
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) {
+    e = current_ctx_id(&id);
+    if (e != cudaSuccess) return e;
+    if (id == 0) return cudaErrorDeviceUninitialized;
+  }
+  a.ctx_id = id;
+  a.ptr = p;
+  *out = p;
   return cudaSuccess;
 }
 
