@@ -3,20 +3,23 @@
 
 A step is one full ``muon_step_batched`` call (momentum + look-ahead + norm,
 10-iteration hybrid Newton–Schulz, scale + decoupled weight decay) over one
-batch of synthetic input.  The default workload is the stacked set:
-64 bf16 1024x1024 matrices with fp32 momentum, fresh Gaussian grads each
-step (sigma 1e-3, per-row scales log-uniform in [0.1, 10]), cycling through
-the 5 steps of grads; spectral scale, mu 0.95, lr 2.7e-4, wd 0.1.
+batch of synthetic input.  The default workload is the largest one, the
+32-layer dense-transformer matrix set (hidden 4096, FFN 14336; per layer
+q, o 4096x4096, k, v 1024x4096, gate, up 14336x4096, down 4096x14336; bf16 W
+and G, fp32 momentum, 6.98 B params), grouped by shape into batched
+Newton–Schulz chains, with Gaussian grads (sigma 1e-3) plus rank-8 spikes;
+spectral scale, mu 0.95, lr 2.7e-4, wd 0.1.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload stack|single|heads|dense|moe|adamw]
+                    [--workload dense|moe|stack|single|heads|adamw]
 
 --workload adamw times the AdamW partition instead (muon_adamw_step over the
 dense 32-layer model's embedding, output head and norm scales: 1.05 B params).
 
-N > 1 runs one process per GPU (torchrun); each rank updates its own copy of
-the workload (matrices are independent units: weak scaling, no collective).
-Rank 0 prints one JSON line.
+N > 1 runs one process per GPU: under torchrun (RANK / WORLD_SIZE set), or,
+launched plainly with --gpus N, through bench.py's own spawner.  Each rank
+updates its own copy of the workload (matrices are independent units: weak
+scaling, no collective on the data path).  Rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -40,9 +43,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["stack", "single", "heads", "dense", "moe", "adamw"],
-                    default="stack")
+                    default="dense")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="stack / single / heads / adamw: seconds of oracle work in cpu_baseline")
+    ap.add_argument("--cpu-per-group", type=int, default=2,
+                    help="dense / moe: matrices per shape group the oracle is timed on")
     ap.add_argument("--prof-steps", type=int, default=50)
     ap.add_argument("--layers", type=int, default=32,
                     help="dense: layers of the matrix set (fewer: a small case, e.g. for ncu)")
@@ -90,21 +96,28 @@ def build_workload(name: str, rank: int):
                           m_dtype="fp32", scale="spectral", seed=2))
 
 
-def device_sets(name: str, rank: int, dev, layers: int = 32, experts: int = 256):
-    """Multi-GB sets drawn on the device: {shape name: (W [B,r,c], G, M)}."""
-    import workloads
+def set_desc(name: str, layers: int = 32, experts: int = 256) -> dict:
     if name == "dense":
-        sets = workloads.dense_layers(seed=3 + 1000 * rank, layers=layers, device=dev)
-        desc = dict(workload=f"dense: {layers} layers x {{q,o 4096^2; k,v 1024x4096; gate,up "
+        return dict(workload=f"dense: {layers} layers x {{q,o 4096^2; k,v 1024x4096; gate,up "
                              f"14336x4096; down 4096x14336}}", matrices=layers * 7,
                     w_dtype="bf16", g_dtype="bf16", m_dtype="fp32", scale="spectral", seed=3,
                     grads="Gaussian 1e-3 + rank-8 spike")
-    else:
-        sets = workloads.moe_experts(seed=4 + 1000 * rank, experts=experts, device=dev)
-        desc = dict(workload=f"moe: {experts} experts x {{up 2048x7168, down 7168x2048}}",
-                    matrices=2 * experts, w_dtype="bf16", g_dtype="bf16", m_dtype="fp32",
-                    scale="spectral", seed=4, grads="1e-3 * Student-t(3)")
-    return sets, desc
+    return dict(workload=f"moe: {experts} experts x {{up 2048x7168, down 7168x2048}}",
+                matrices=2 * experts, w_dtype="bf16", g_dtype="bf16", m_dtype="fp32",
+                scale="spectral", seed=4, grads="1e-3 * Student-t(3)")
+
+
+def draw_set(name: str, rank: int, dev, layers: int = 32, experts: int = 256):
+    """A multi-GB set drawn on the device: {member name: (W [B,r,c], G, M)}."""
+    import workloads
+    if name == "dense":
+        return workloads.dense_layers(seed=3 + 1000 * rank, layers=layers, device=dev)
+    return workloads.moe_experts(seed=4 + 1000 * rank, experts=experts, device=dev)
+
+
+def device_sets(name: str, rank: int, dev, layers: int = 32, experts: int = 256):
+    """Multi-GB sets drawn on the device: {shape name: (W [B,r,c], G, M)}."""
+    return draw_set(name, rank, dev, layers, experts), set_desc(name, layers, experts)
 
 
 def set_groups(m, sets):
@@ -216,22 +229,52 @@ def oracle_sample(wl, seconds: float, min_units: int = 1):
     return params / dt, done, dt
 
 
-def oracle_sample_sets(sets, seconds: float):
-    """Oracle on matrices of a device-drawn set (copied to the host one by one),
-    smallest shape first, until `seconds` have passed (at least one matrix)."""
+def shape_groups(sets) -> dict:
+    """{(rows, cols): [(name, index), ...]}: the matrices of a device-drawn set
+    by shape (the groups muon_group_by_shape forms), in order of first
+    appearance."""
+    out = {}
+    for nm, (W, _, _) in sets.items():
+        key = (int(W.shape[1]), int(W.shape[2]))
+        out.setdefault(key, []).extend((nm, b) for b in range(W.shape[0]))
+    return out
+
+
+def oracle_matrix_seconds(sets, nm: str, b: int) -> float:
+    """Wall time of one float64 oracle Muon step on matrix b of set member nm
+    (the host copies are made before the clock starts)."""
     import numpy as np
     import oracle
-    hp = oracle.MuonHyper()
-    order = sorted(sets.items(), key=lambda kv: kv[1][0].shape[1] * kv[1][0].shape[2])
-    nm, (W, G, M) = order[0]
-    done, params, t0 = 0, 0, time.perf_counter()
-    while done < 1 or (time.perf_counter() - t0 < seconds and done < W.shape[0]):
-        oracle.muon_step(W[done].float().cpu().numpy().astype(np.float64),
-                         G[done].float().cpu().numpy().astype(np.float64),
-                         M[done].cpu().numpy().astype(np.float64), hp)
-        params += W[done].numel()
-        done += 1
-    return params / (time.perf_counter() - t0), done, time.perf_counter() - t0, W.shape[1], W.shape[2]
+    W, G, M = sets[nm]
+    w, g, mm = (x[b].float().cpu().numpy().astype(np.float64) for x in (W, G, M))
+    t0 = time.perf_counter()
+    oracle.muon_step(w, g, mm, oracle.MuonHyper())
+    return time.perf_counter() - t0
+
+
+def extrapolate(counts: dict, seconds: dict) -> tuple:
+    """Whole-set oracle time from per-shape samples: sum over shapes of the
+    shape's matrix count x its mean sampled time per matrix.
+    counts {(r, c): matrices}, seconds {(r, c): [sampled seconds, ...]}.
+    Returns (params/s, extrapolated seconds per step)."""
+    params = sum(r * c * n for (r, c), n in counts.items())
+    total = sum(n * (sum(seconds[k]) / len(seconds[k])) for k, n in counts.items())
+    return params / total, total
+
+
+def oracle_sample_sets(sets, per_group: int):
+    """Oracle on `per_group` matrices of every shape group of a device-drawn
+    set, extrapolated to the whole set by the groups' matrix counts (the cost
+    per parameter grows with the Gram size, so every shape is timed)."""
+    groups = shape_groups(sets)
+    secs = {k: [oracle_matrix_seconds(sets, nm, b) for nm, b in mem[:max(1, per_group)]]
+            for k, mem in groups.items()}
+    value, total = extrapolate({k: len(v) for k, v in groups.items()}, secs)
+    timed = sum(sum(v) for v in secs.values())
+    sample = (", ".join(f"{len(secs[k])} of {len(groups[k])} {k[0]}x{k[1]}" for k in groups) +
+              f" (one Muon step each, float64 NumPy, {timed:.1f} s); whole-set time "
+              f"extrapolated by each shape's matrix count: {total:.0f} s per step")
+    return value, sample
 
 
 def cpu_cores():
@@ -265,10 +308,72 @@ def job_value(steps: int, params_per_rank: int, world: int, ms_max: float) -> fl
     return world * steps * params_per_rank / (ms_max / 1e3)
 
 
+def reference_line(args, value: float, dt: float, desc: dict, sample: str) -> dict:
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": desc,
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def step_plan(n_groups: int, steps: int, cheapest: int) -> list:
+    """Shape groups the oracle runs in each timed step of the reference arm:
+    every group at least once over the run (one matrix each), the remaining
+    steps on the cheapest group; with fewer steps than groups a step takes
+    several."""
+    if steps >= n_groups:
+        return [[i] if i < n_groups else [cheapest] for i in range(steps)]
+    return [list(range(i, n_groups, steps)) for i in range(steps)]
+
+
+def run_reference_sets(args):
+    """Reference arm on a device-drawn set: each step times the oracle on whole
+    matrices of one layer's (expert's) draw of the set, per step_plan; the
+    params/s is the whole set's, extrapolated from the per-shape times by each
+    shape's matrix count."""
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    small = draw_set(args.workload, 0, dev, layers=1, experts=1)
+    groups = shape_groups(small)
+    keys = list(groups)
+    scale = args.layers if args.workload == "dense" else args.experts
+    counts = {k: len(groups[k]) * scale for k in keys}
+    cost = lambda k: min(k) ** 2 * max(k)
+    cheapest = min(range(len(keys)), key=lambda i: cost(keys[i]))
+    for _ in range(args.warmup):
+        nm, b = groups[keys[cheapest]][0]
+        oracle_matrix_seconds(small, nm, b)
+    secs = {k: [] for k in keys}
+    nxt = {k: 0 for k in keys}
+    t0 = time.perf_counter()
+    for grp in step_plan(len(keys), args.steps, cheapest):
+        for gi in grp:
+            k = keys[gi]
+            nm, b = groups[k][nxt[k] % len(groups[k])]
+            nxt[k] += 1
+            secs[k].append(oracle_matrix_seconds(small, nm, b))
+    dt = time.perf_counter() - t0
+    value, total = extrapolate(counts, secs)
+    sample = ("per step one matrix (float64 NumPy oracle Muon step), every shape group at least "
+              "once, the other steps on the cheapest: " +
+              ", ".join(f"{len(secs[k])} x {k[0]}x{k[1]}" for k in keys) +
+              f"; whole-set time extrapolated by each shape's matrix count: {total:.0f} s")
+    print(json.dumps(reference_line(args, value, dt, set_desc(args.workload, args.layers,
+                                                                args.experts), sample)),
+          flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return 0
+    if args.workload in ("dense", "moe"):
+        return run_reference_sets(args)
     wl = build_workload(args.workload, 0)
     per_step = 120.0 / max(1, args.steps + args.warmup)   # whole run ~2 min (>= 1 matrix/step)
     for _ in range(args.warmup):
@@ -283,15 +388,7 @@ def run_reference(args):
     value = params / dt
     rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
     sample = f"{units} matrices of {rows}x{cols} over {args.steps} steps (float64 NumPy oracle)"
-    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
-           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl["desc"],
-           "cpu_baseline": {"value": value, "unit": "params/s", "cores": cpu_cores(),
-                            "kind": "oracle", "sample": sample},
-           "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
-                   "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    print(json.dumps(reference_line(args, value, dt, wl["desc"], sample)), flush=True)
     return 0
 
 
@@ -303,7 +400,7 @@ def kernel_source_hash(files=("ns_gemm.cu", "ptx.cuh")):
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel: str, summary="ns_gemm_traffic.json", files=("ns_gemm.cu", "ptx.cuh")):
+def read_traffic(kernel: str, summary="ns_gemm_traffic_stack.json", files=("ns_gemm.cu", "ptx.cuh")):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", summary)
@@ -317,6 +414,106 @@ def read_traffic(kernel: str, summary="ns_gemm_traffic.json", files=("ns_gemm.cu
     if not e:
         return None
     return e.get("dram_bytes_per_launch_full_workload")
+
+
+def pick_peak(peaks: dict, timed_s: float) -> tuple:
+    """Tensor peak for the roofline: the sustained measurement (a seconds-long
+    loop under the power cap) for kernels timed inside a timed region of a
+    second or more, the burst one for a short region."""
+    if timed_s >= 1.0:
+        return peaks["bf16_tflops_sustained"], "sustained"
+    return peaks["bf16_tflops"], "burst"
+
+
+def pinned_like(tensors):
+    """Pinned host copies (uninitialised) of `tensors`, carved out of one
+    pinned buffer."""
+    import torch
+    sizes = [t.numel() * t.element_size() for t in tensors]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    buf = torch.empty(max(1, o), dtype=torch.uint8, pin_memory=True)
+    return [buf[a:a + n].view(t.dtype).view(t.shape) for a, n, t in zip(offs, sizes, tensors)]
+
+
+def e2e_leg(m, stream, groups_of, grads, W_list, hp, ws, sched, n_e, world, dev, barrier):
+    """End to end through host buffers, pipelined the way a training loop fed
+    from host memory runs: step i's gradients (pinned host -> one of two
+    device slots, on a copy stream) upload while step i - 1 computes, and step
+    i's W leaves for pinned host memory from a device snapshot taken right
+    after the step, while step i + 1 computes.  Every step's uploads and
+    downloads lie inside the timed region (the first upload waits for its
+    start, its end waits for the last download); each step's status word is
+    saved on the device and all are checked at the end.
+    grads: per step of the input cycle, the list of gradient tensors;
+    groups_of(list of gradient tensors) -> the step's muon groups."""
+    import torch
+    Gh = []
+    for gl in grads:
+        hs = pinned_like(gl)
+        for h, g in zip(hs, gl):
+            h.copy_(g)
+        Gh.append(hs)
+    slots = [[torch.empty_like(g) for g in grads[0]] for _ in range(2)]
+    egs = [groups_of(sl) for sl in slots]
+    Wsnap = [torch.empty_like(w) for w in W_list]
+    Wh = pinned_like(W_list)
+    status_word = ws[:4].view(torch.int32)
+    flags_d = torch.zeros(n_e, dtype=torch.int32, device=dev)
+    flags_h = torch.empty(n_e, dtype=torch.int32).pin_memory()
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_g = [torch.cuda.Event() for _ in range(n_e)]
+    ev_done = [torch.cuda.Event() for _ in range(n_e)]
+    ev_out = [torch.cuda.Event() for _ in range(n_e)]
+    for i in range(2):
+        for d, h in zip(slots[i], Gh[i % len(Gh)]):
+            d.copy_(h, non_blocking=True)
+        m.muon_step_batched(egs[i], hp, ws, sched)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n_e):
+        slot = i % 2
+        with torch.cuda.stream(s_h2d):
+            s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])  # slot free again
+            for d, h in zip(slots[slot], Gh[i % len(Gh)]):
+                d.copy_(h, non_blocking=True)
+            ev_g[i].record(s_h2d)
+        stream.wait_event(ev_g[i])
+        m.muon_step_batched(egs[slot], hp, ws, sched)
+        flags_d[i:i + 1].copy_(status_word)
+        if i > 0:
+            stream.wait_event(ev_out[i - 1])  # the snapshot has left for the host
+        for d, w in zip(Wsnap, W_list):
+            d.copy_(w)
+        ev_done[i].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_done[i])
+            for h, d in zip(Wh, Wsnap):
+                h.copy_(d, non_blocking=True)
+            ev_out[i].record(s_d2h)
+    stream.wait_event(ev_out[n_e - 1])
+    flags_h.copy_(flags_d, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    if int(flags_h.abs().sum()) != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
+    P = sum(w.numel() for w in W_list)
+    return {"value": job_value(n_e, P, world, e_ms), "unit": "params/s",
+            "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in slots[0])),
+            "d2h_bytes_per_step": int(sum(w.numel() * w.element_size() for w in Wh) + 4),
+            "steps": n_e, "ms_per_step": e_ms / n_e, "wall_s": round(wall, 4),
+            "path": "pinned host G -> device (copy stream, overlapping the previous step), "
+                    "muon_step_batched, W snapshot on the device -> pinned host (copy "
+                    "stream, overlapping the next step); each step's status word saved "
+                    "on the device and checked after the last step"}
 
 
 def run_ours(args):
@@ -333,11 +530,18 @@ def run_ours(args):
     m.load_library()
     peaks, peak_src = load_peaks()
 
+    sets = None
     if args.workload in ("dense", "moe"):
         sets, desc = device_sets(args.workload, rank, dev, args.layers, args.experts)
         groups = [set_groups(m, sets)]
         P = int(sum(W.numel() for W, _, _ in sets.values()))
         wl = {"kind": args.workload, "sets": sets, "desc": desc}
+        names = list(sets)
+
+        def groups_of(gl):
+            return set_groups(m, {nm: (sets[nm][0], g, sets[nm][2]) for nm, g in zip(names, gl)})
+        step_grads = [[sets[nm][1] for nm in names]]
+        W_list = [sets[nm][0] for nm in names]
     else:
         wl = build_workload(args.workload, rank)
         Wd = wl["W"].to(dev)
@@ -345,6 +549,11 @@ def run_ours(args):
         Gd = [g.to(dev) for g in wl["grads"]]
         groups = make_groups(m, wl, Wd, Md, Gd)
         P = n_params(wl)
+
+        def groups_of(gl):
+            return make_groups(m, wl, Wd, Md, gl)[0]
+        step_grads = [[g] for g in Gd]
+        W_list = [Wd]
     hp = m.hparams()
     sched = None
     merge = args.merge == 1 and args.workload in ("dense", "moe")
@@ -380,13 +589,14 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
     ms = start.elapsed_time(stop)
+    clocks = clk.summary()
     launches = int(sum(v["launches"] for v in m.muon_profile_query().values()))
     code, flags = m.muon_get_status(ws)
     if code != m.MUON_OK or flags:
         raise RuntimeError(f"device status {code} flags {flags:#x} after timed steps")
     # Per-kernel pass: the same steps again with a CUDA event pair recorded on
     # the launching stream around every kernel (roofline and kernel table).
-    prof_steps = max(1, min(args.steps, args.prof_steps))
+    prof_steps = max(1, min(args.steps, args.prof_steps, 5 if sets is not None else args.prof_steps))
     m.muon_profile_reset()
     m.muon_profile_enable(True)
     torch.cuda.synchronize()
@@ -408,23 +618,26 @@ def run_ours(args):
     dom = max(timed, key=lambda k: timed[k]["total_ms"])
     d = timed[dom]
     avg_s = d["total_ms"] / d["launches"] / 1e3
+    timing = f"event pair per launch, {prof_steps} profiled steps after the timed region"
+    traffic_file = f"ns_gemm_traffic_{args.workload}.json"
     if dom.startswith("ns_"):
         per_launch = d["alg_flops"] / d["launches"]
         achieved = per_launch / avg_s / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "timing": f"event pair per launch, {prof_steps} profiled steps after the timed region",
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"],
+        peak, peak_kind = pick_peak(peaks, ms / 1e3)
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "timing": timing,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "frac_burst_peak": achieved / peaks["bf16_tflops"],
                 "frac_sustained_peak": achieved / peaks["bf16_tflops_sustained"],
                 "alg_flops_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
-                "traffic": read_traffic(dom), "peak_source": f"{peak_src} bf16 burst"}
+                "traffic": read_traffic(dom, traffic_file),
+                "peak_source": f"{peak_src} bf16 {peak_kind} (timed region {ms / 1e3:.2f} s)"}
     else:
         per_launch = d["alg_bytes"] / d["launches"]
         achieved = per_launch / avg_s / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "timing": f"event pair per launch, {prof_steps} profiled steps after the timed region",
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                "alg_bytes_per_launch": per_launch, "avg_launch_ms": avg_s * 1e3,
-                "peak_source": f"{peak_src} copy"}
+                "timing": timing, "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": None, "alg_bytes_per_launch": per_launch,
+                "avg_launch_ms": avg_s * 1e3, "peak_source": f"{peak_src} copy"}
     kernels = {}
     for k, v in timed.items():
         e = {"launches": v["launches"], "total_ms": round(v["total_ms"], 4),
@@ -435,92 +648,50 @@ def run_ours(args):
             e["gbs"] = round(v["alg_bytes"] / (v["total_ms"] / 1e3) / 1e9, 1)
             e["hbm_frac_of_measured"] = round(e["gbs"] / peaks["hbm_gbs"], 3)
         kernels[k] = e
+    # ---- the elementwise pass before Newton–Schulz (momentum, look-ahead,
+    # norm partials) against HBM, at the minimal byte count: G + M read and
+    # written + X written once (12 B per bf16-G parameter); the library's own
+    # count adds the iterate's 2-byte residual plane
+    elementwise = None
+    if "prepare" in timed:
+        pe = timed["prepare"]
+        g_bytes = 4 if args.workload == "single" else 2
+        min_bytes = (g_bytes + 8 + 2) * P * prof_steps
+        gbs = min_bytes / (pe["total_ms"] / 1e3) / 1e9
+        elementwise = {"kernel": "prepare", "bound": "hbm", "bytes_per_param": g_bytes + 10,
+                       "gbs": gbs, "frac_of_measured_copy": gbs / peaks["hbm_gbs"],
+                       "frac_of_8tbs": gbs / 8000.0,
+                       "library_count": {"bytes_per_param": g_bytes + 12,
+                                         "gbs": kernels["prepare"]["gbs"],
+                                         "frac_of_measured_copy":
+                                             kernels["prepare"]["hbm_frac_of_measured"]}}
 
     # ---- end to end: host buffers, copies inside the timed region ------------
     e2e = None
-    if args.e2e_steps > 0 and args.workload in ("dense", "moe"):
-        e2e = {"value": None, "unit": "params/s", "skipped": "multi-GB device-drawn set; the "
-               "end-to-end leg runs on the stacked workload"}
-    elif args.e2e_steps > 0:
-        # Pipelined the way a training loop fed from host memory runs: step
-        # i's gradient upload (its own copy stream, two device slots) overlaps
-        # step i - 1, and step i's W goes to the host from a device snapshot
-        # taken on the compute stream right after the step, while step i + 1
-        # runs.  Every step's uploads and downloads lie inside the timed region
-        # (the first upload waits for its start, its end waits for the last
-        # download); each step's status word is saved on the device and all are
-        # read back and checked at the end.
-        n_e = args.e2e_steps
-        Gh = [g.pin_memory() for g in wl["grads"]]
-        Gslots = [torch.empty_like(Gd[0]) for _ in range(2)]
-        Wsnap = torch.empty_like(Wd)
-        Wh = torch.empty(Wd.shape, dtype=Wd.dtype).pin_memory()
-        egs = [make_groups(m, wl, Wd, Md, [g])[0] for g in Gslots]
-        status_word = ws[:4].view(torch.int32)
-        flags_d = torch.zeros(n_e, dtype=torch.int32, device=dev)
-        flags_h = torch.empty(n_e, dtype=torch.int32).pin_memory()
-        s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        ev_g = [torch.cuda.Event() for _ in range(n_e)]
-        ev_done = [torch.cuda.Event() for _ in range(n_e)]
-        ev_out = [torch.cuda.Event() for _ in range(n_e)]
-        for i in range(2):
-            Gslots[i].copy_(Gh[i % len(Gh)], non_blocking=True)
-            m.muon_step_batched(egs[i], hp, ws, sched)
-        torch.cuda.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(n_e):
-            slot = i % 2
-            with torch.cuda.stream(s_h2d):
-                s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])  # slot free again
-                Gslots[slot].copy_(Gh[i % len(Gh)], non_blocking=True)
-                ev_g[i].record(s_h2d)
-            stream.wait_event(ev_g[i])
-            m.muon_step_batched(egs[slot], hp, ws, sched)
-            flags_d[i:i + 1].copy_(status_word)
-            if i > 0:
-                stream.wait_event(ev_out[i - 1])  # the snapshot has left for the host
-            Wsnap.copy_(Wd)
-            ev_done[i].record(stream)
-            with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(ev_done[i])
-                Wh.copy_(Wsnap, non_blocking=True)
-                ev_out[i].record(s_d2h)
-        stream.wait_event(ev_out[n_e - 1])
-        flags_h.copy_(flags_d, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-        barrier()
-        e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-        if int(flags_h.abs().sum()) != 0:
-            raise RuntimeError("device status set during the end-to-end steps")
-        e2e = {"value": job_value(n_e, P, world, e_ms), "unit": "params/s",
-               "h2d_bytes_per_step": int(Gslots[0].numel() * Gslots[0].element_size()),
-               "d2h_bytes_per_step": int(Wh.numel() * Wh.element_size() + 4),
-               "steps": n_e, "wall_s": round(wall, 4),
-               "path": "pinned host G -> device (copy stream, overlapping the previous step), "
-                       "muon_step_batched, W snapshot on the device -> pinned host (copy "
-                       "stream, overlapping the next step); each step's status word saved "
-                       "on the device and checked after the last step"}
+    if args.e2e_steps > 0:
+        n_e = args.e2e_steps if sets is None else max(3, min(args.e2e_steps, 8))
+        e2e = e2e_leg(m, stream, groups_of, step_grads, W_list, hp, ws, sched, n_e, world, dev,
+                      barrier)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
-    if "sets" in wl:
-        cpu_v, cpu_n, cpu_dt, rows, cols = oracle_sample_sets(wl["sets"], args.cpu_seconds)
-    else:
-        cpu_v, cpu_n, cpu_dt = oracle_sample(wl, args.cpu_seconds)
-        rows, cols = wl["desc"]["rows"], wl["desc"]["cols"]
-    clocks = clk.summary()
+    cpu = None
+    if world == 1:
+        if sets is not None:
+            cpu_v, sample = oracle_sample_sets(sets, args.cpu_per_group)
+        else:
+            cpu_v, cpu_n, cpu_dt = oracle_sample(wl, args.cpu_seconds)
+            sample = (f"{cpu_n} matrices of {wl['desc']['rows']}x{wl['desc']['cols']}, one Muon "
+                      f"step each, float64 NumPy, {cpu_dt:.1f} s")
+        cpu = {"value": cpu_v, "unit": "params/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": sample}
     desc = dict(wl["desc"])
     desc["ns_precision"] = {"bf16": "bf16 (MUON_NS_BF16)",
                             "x3": "split-bf16 (MUON_NS_BF16X3, three products per GEMM)"}[args.prec]
-    if wl["kind"] in ("dense", "moe"):
+    if sets is not None:
         desc["merge_groups"] = bool(merge)
     desc.update(parallelism=f"replicas x{world} (independent matrices, no collective)",
                 l2={"stack": "inputs larger than L2: per step 128 MiB G + 128 MiB W + 256 MiB M "
@@ -531,15 +702,12 @@ def run_ours(args):
     out = {"metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-           "data": "synthetic (seeded Gaussian grads, per-row scales)", "config": desc,
+           "data": "synthetic (seeded, drawn on the device)" if sets is not None
+                   else "synthetic (seeded, drawn on the host)", "config": desc,
            "ns_tflops": ns_tflops,
            "ns_frac_of_bf16_peak": ns_tflops / peaks["bf16_tflops"] if ns_tflops else None,
-           "roofline": roof, "kernels": kernels,
-           "cpu_baseline": {"value": cpu_v, "unit": "params/s", "cores": cpu_cores(),
-                            "kind": "oracle",
-                            "sample": f"{cpu_n} matrices of {rows}x{cols}, one Muon step each, "
-                                      f"float64 NumPy, {cpu_dt:.1f} s"},
-           "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+           "roofline": roof, "elementwise": elementwise, "kernels": kernels,
+           "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
            "peaks": dict(peaks, source=peak_src)}
     print(json.dumps(out), flush=True)
     if world > 1:
@@ -752,14 +920,60 @@ def run_adamw(args):
     return 0
 
 
-def main():
-    args = parse()
-    sys.path.insert(0, ROOT)
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, target, args):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    sys.exit(target(args) or 0)
+
+
+def spawn_ranks(n: int, target, args, timeout_s: float = 3600.0) -> int:
+    """Run target(args) as n processes, one per rank (GPU), with the
+    environment a torchrun launch gives them (RANK, LOCAL_RANK, WORLD_SIZE,
+    MASTER_ADDR 127.0.0.1, a free MASTER_PORT).  Returns the first non-zero
+    exit code, else 0."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    port = free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, n, port, target, args)) for r in range(n)]
+    for p in procs:
+        p.start()
+    rc = 0
+    for p in procs:
+        p.join(timeout_s)
+        if p.exitcode is None:
+            p.kill()
+            p.join()
+        code = p.exitcode if p.exitcode is not None else 1
+        if code != 0 and rc == 0:
+            rc = code
+    return rc
+
+
+def run(args) -> int:
     if args.workload == "adamw":
         return run_adamw(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
+
+
+def main():
+    args = parse()
+    sys.path.insert(0, ROOT)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # launched plainly: one process per GPU from here (torchrun sets WORLD_SIZE)
+        return spawn_ranks(args.gpus, run, args)
+    return run(args)
 
 
 if __name__ == "__main__":

@@ -1,7 +1,8 @@
 """The bench's host logic on CPU: two gloo ranks on 127.0.0.1 check the
 cross-rank reduction of the timed region (max over ranks) and the whole-job
-value; the reference arm does no work on ranks other than 0, and on rank 0
-prints one contract line."""
+value, and that bench.py's own spawner starts one process per rank; the
+reference arm does no work on ranks other than 0, on rank 0 prints one
+contract line, and extrapolates a set's oracle time from every shape."""
 import os
 import socket
 
@@ -117,3 +118,87 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path):
     p.write_text(json.dumps(dict(entry, source_hash="0" * 16)))
     assert bench.read_traffic("ns_gram_poly", summary=str(p)) is None
     assert bench.read_traffic("ns_gram_poly", summary=str(tmp_path / "absent.json")) is None
+
+
+def _stub_step(args):
+    """Stands for one rank's bench run: joins the gloo group the spawner's
+    environment describes, reduces its timed region, rank 0 prints one line."""
+    import json
+    rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+    assert int(os.environ["LOCAL_RANK"]) == rank and os.environ["MASTER_ADDR"] == "127.0.0.1"
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = bench.max_over_ranks(10.0 + rank, world)
+    if rank == 0:
+        print(json.dumps({"n_gpus": world, "ms": ms,
+                          "value": bench.job_value(args.steps, 100, world, ms)}), flush=True)
+    dist.barrier()
+    dist.destroy_process_group()
+    return 0
+
+
+def test_spawner_launches_one_process_per_rank(capfd):
+    import argparse
+    import json
+    args = argparse.Namespace(steps=4, gpus=2)
+    assert bench.spawn_ranks(2, _stub_step, args, timeout_s=120) == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["ms"] == 11.0
+    assert d["value"] == pytest.approx(2 * 4 * 100 / 0.011)
+
+
+def test_plain_launch_with_several_gpus_goes_through_the_spawner(monkeypatch):
+    seen = {}
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(bench, "spawn_ranks", lambda n, target, args: seen.update(n=n) or 0)
+    monkeypatch.setattr(bench, "run", lambda args: pytest.fail("ran in the launching process"))
+    monkeypatch.setattr("sys.argv", ["bench.py", "--gpus", "3", "--steps", "2"])
+    assert bench.main() == 0 and seen == {"n": 3}
+    # under torchrun (WORLD_SIZE set) the process is already one rank
+    monkeypatch.setenv("WORLD_SIZE", "3")
+    monkeypatch.setattr(bench, "run", lambda args: 0)
+    monkeypatch.setattr(bench, "spawn_ranks", lambda *a: pytest.fail("spawned under torchrun"))
+    assert bench.main() == 0
+
+
+def test_step_plan_covers_every_group():
+    plan = bench.step_plan(4, 6, cheapest=1)
+    assert plan == [[0], [1], [2], [3], [1], [1]]
+    plan = bench.step_plan(4, 3, cheapest=1)       # fewer steps than groups
+    assert sorted(g for step in plan for g in step) == [0, 1, 2, 3] and len(plan) == 3
+
+
+def test_extrapolation_weights_shapes_by_count():
+    counts = {(4, 8): 10, (16, 16): 2}
+    secs = {(4, 8): [1.0, 3.0], (16, 16): [5.0]}
+    v, total = bench.extrapolate(counts, secs)
+    assert total == pytest.approx(10 * 2.0 + 2 * 5.0)
+    assert v == pytest.approx((10 * 32 + 2 * 256) / total)
+
+
+def test_reference_arm_on_a_set_prints_the_extrapolated_line(monkeypatch, capsys):
+    """The set path of the reference arm on a tiny stand-in set (two shapes),
+    so that it runs on CPU in seconds: one JSON line, every shape sampled."""
+    import argparse
+    import json
+
+    import torch
+
+    def tiny(name, rank, dev, layers=1, experts=1):
+        g = torch.Generator().manual_seed(0)
+        mk = lambda r, c: ((torch.randn(1, r, c, generator=g) * 0.02).to(torch.bfloat16),
+                           (torch.randn(1, r, c, generator=g) * 1e-3).to(torch.bfloat16),
+                           torch.zeros(1, r, c))
+        return {"a": mk(16, 32), "b": mk(16, 32), "c": mk(48, 16)}
+    monkeypatch.setattr(bench, "draw_set", tiny)
+    args = argparse.Namespace(steps=3, warmup=1, gpus=1, workload="dense", layers=32,
+                              experts=256)
+    assert bench.run_reference(args) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 3
+    assert d["config"]["workload"].startswith("dense: 32 layers")
+    assert "16x32" in d["cpu_baseline"]["sample"] and "48x16" in d["cpu_baseline"]["sample"]
+    assert "extrapolated" in d["cpu_baseline"]["sample"]
