@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="stack / single / heads / adamw: seconds of oracle work in cpu_baseline")
     ap.add_argument("--cpu-per-group", type=int, default=2,
-                    help="dense / moe: matrices per shape group the oracle is timed on")
+                    help="dense / moe: matrices per shape group the oracle is timed on "
+                         "(0: no cpu_baseline, for profiling runs)")
     ap.add_argument("--prof-steps", type=int, default=50)
     ap.add_argument("--layers", type=int, default=32,
                     help="dense: layers of the matrix set (fewer: a small case, e.g. for ncu)")
@@ -679,7 +680,7 @@ def run_ours(args):
         return 0
 
     cpu = None
-    if world == 1:
+    if world == 1 and not (sets is not None and args.cpu_per_group <= 0):
         if sets is not None:
             cpu_v, sample = oracle_sample_sets(sets, args.cpu_per_group)
         else:

@@ -237,6 +237,16 @@ muon_status_t muon_set_wait_timeout_ns(uint64_t ns);
 muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
                                       uint64_t timeout_ns, muon_stream_t stream);
 
+/* Co-scheduling check: launches `blocks` blocks of one warp, each holding
+ * `smem_bytes` of dynamic shared memory (at most 227 KiB), that wait `ns`
+ * nanoseconds by the GPU's global timer (at most 1 s) and exit.  Run on one
+ * stream while a step runs on another, it keeps most SMs from the step's
+ * kernels for a bounded time, the way concurrent work (a communication
+ * kernel, another model's step) does in a shared job; used to test that the
+ * step still completes within its bounded waits.  The pages have no
+ * counterpart to it. */
+muon_status_t muon_occupy_sms(int blocks, size_t smem_bytes, uint64_t ns, muon_stream_t stream);
+
 /* Allocation-free variant of newton_schulz_batched.  The pages have no
  * counterpart to it; it exists for callers that cannot obtain a workspace
  * from cudaMalloc: code inside a framework whose caching allocator owns all

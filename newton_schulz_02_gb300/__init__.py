@@ -108,6 +108,7 @@ PROTOTYPES = {
     "muon_get_status": (c_int, [c_void_p, c_void_p, POINTER(c_uint32)]),
     "muon_set_wait_timeout_ns": (c_int, [c_uint64]),
     "muon_check_wait_timeout": (c_int, [c_void_p, c_size_t, c_uint64, c_void_p]),
+    "muon_occupy_sms": (c_int, [c_int, c_size_t, c_uint64, c_void_p]),
     "muon_profile_enable": (c_int, [c_int]),
     "muon_profile_reset": (c_int, []),
     "muon_profile_query": (c_int, [POINTER(muon_kernel_stats_t), c_int, POINTER(c_int)]),
@@ -365,6 +366,13 @@ def muon_set_wait_timeout_ns(ns: int) -> None:
 def muon_check_wait_timeout(ws: torch.Tensor, timeout_ns: int, stream=None) -> None:
     _check(load_library().muon_check_wait_timeout(ws.data_ptr(), ws.numel(), int(timeout_ns),
                                                   _stream(stream)), "muon_check_wait_timeout")
+
+
+def muon_occupy_sms(blocks: int, smem_bytes: int, ns: int, stream=None) -> None:
+    """Hold `blocks` SMs (one block of `smem_bytes` shared memory each) for
+    `ns` nanoseconds on `stream`; see include/muon.h."""
+    _check(load_library().muon_occupy_sms(int(blocks), int(smem_bytes), int(ns), _stream(stream)),
+           "muon_occupy_sms")
 
 
 def muon_profile_enable(on: bool) -> None:

@@ -375,6 +375,18 @@ __global__ void k_wait_timeout_check(uint32_t* status, uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// Holds an SM for `ns` nanoseconds by the global timer, then exits: every
+// block takes the dynamic shared memory it is launched with, so that no
+// other large-shared-memory block fits beside it.
+__global__ void k_occupy(uint64_t ns) {
+  extern __shared__ uint8_t hold[];
+  if (threadIdx.x == 0) {
+    hold[0] = 0;
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ns) __nanosleep(1000);
+  }
+}
+
 }  // namespace
 
 // Blocks per matrix: a function of the shape only (determinism across batch sizes).
@@ -437,6 +449,14 @@ cudaError_t launch_apply(const ApplyArgs& a, cudaStream_t st) {
                                : cudaLaunchKernelEx(&cfg, k_apply_wide, a);
   prof_end(kKindApply, st, 0.0, elems * per);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_occupy(int blocks, size_t smem_bytes, uint64_t ns, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_occupy, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  k_occupy<<<blocks, 32, smem_bytes, st>>>(ns);
   return cudaGetLastError();
 }
 

@@ -139,6 +139,8 @@ struct NsChainArgs {
   float* partial;       // split-K Gram slices, gram_ksplit(...) * batch * n_pad^2 fp32, or nullptr
   int* gp_ctr;          // [batch] counters for the fused Gram + polynomial launches (zero on
                         // entry), or nullptr
+  int* gp_tick;         // [kGpMaxLaunches] ticket counters of those launches, then (at
+  int* gp_log;          // gp_log) their ticket log; both zero on entry, or nullptr
   uint32_t* status;
   uint64_t timeout_ns;
 };
@@ -190,6 +192,7 @@ cudaError_t launch_adamw(AdamWGroupArgs* groups, int n_groups, const AdamWScalar
                          uint32_t* flags, cudaStream_t st);
 
 cudaError_t launch_wait_timeout_check(uint32_t* status, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t launch_occupy(int blocks, size_t smem_bytes, uint64_t ns, cudaStream_t st);
 
 // Whether the chain's last iterate (after `iters` iterations) carries a lo plane.
 bool ns_final_has_lo(int iters, bool x3);
@@ -203,6 +206,18 @@ bool ns_final_fused(int iters, bool x3);
 // unsplit); a function of the shape alone, so that a matrix's result does not
 // depend on the batch it is in.
 int gram_ksplit(int n_pad, int m_pad, bool x3);
+
+// Fused Gram + polynomial launches (bf16 precision, n_pad a multiple of 256)
+// hand their work units out by tickets: per chain at most kGpMaxLaunches of
+// them (later iterations launch the Gram and the polynomial separately), each
+// with at most kGpMaxClusters CTA pairs.
+constexpr int kGpMaxLaunches = 64;
+constexpr int kGpMaxClusters = 128;
+
+// Ints of workspace the ticket counters and log of a chain take (0 where the
+// chain never fuses): kGpMaxLaunches counters, then kGpMaxClusters rows of
+// (tickets of one launch + 2) entries.  Zeroed once per chain.
+size_t gram_poly_log_ints(int batch, int n_pad, bool x3);
 
 // Runs the whole chain; the final iterate is left in X0 if the number of
 // iterations is even, else in X1.  Returns cudaErrorNotSupported when the

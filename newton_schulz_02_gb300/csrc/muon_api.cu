@@ -48,6 +48,8 @@ struct Layout {
   size_t x0 = 0, x1 = 0, a = 0, b = 0, pdiag = 0, partials = 0, inv_s = 0, skip = 0, total = 0;
   size_t kslices = 0;     // split-K Gram slices (fp32), when gram_ksplit(...) > 1
   size_t gp_ctr = 0;      // [batch] int: Gram arrivals of the fused Gram + polynomial launches
+  size_t gp_log = 0;      // ticket counters and log of those launches (gp_log_bytes; 0 = none)
+  size_t gp_log_bytes = 0;
   int ksplit = 1;
 };
 
@@ -78,6 +80,8 @@ Layout layout_for(int batch, int n_pad, int m_pad, int parts, bool x3) {
   L.inv_s = off; off += align256(static_cast<size_t>(batch) * 4);
   L.skip = off; off += align256(static_cast<size_t>(batch));
   L.gp_ctr = off; off += align256(static_cast<size_t>(batch) * 4);
+  L.gp_log_bytes = gram_poly_log_ints(batch, n_pad, x3) * 4;
+  L.gp_log = off; off += align256(L.gp_log_bytes);
   L.ksplit = gram_ksplit(n_pad, m_pad, x3);
   if (L.ksplit > 1) {
     L.kslices = off;
@@ -215,6 +219,8 @@ muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
   fa.normalize = normalize;
   fa.status = status;
   fa.gp_ctr = reinterpret_cast<int*>(ws + L.gp_ctr);
+  if (L.gp_log_bytes > 0 && cudaMemsetAsync(ws + L.gp_log, 0, L.gp_log_bytes, st) != cudaSuccess)
+    return MUON_ERR_CUDA;
   cudaError_t e = launch_finalize(fa, st);
   if (e != cudaSuccess) return MUON_ERR_CUDA;
 
@@ -240,6 +246,10 @@ muon_status_t run_chain_tail(const Layout& L, char* ws, int batch, int n, int m,
   na.sq_lo_off = L.sq_lo_off;
   na.partial = L.ksplit > 1 ? reinterpret_cast<float*>(ws + L.kslices) : nullptr;
   na.gp_ctr = reinterpret_cast<int*>(ws + L.gp_ctr);
+  if (L.gp_log_bytes > 0) {
+    na.gp_tick = reinterpret_cast<int*>(ws + L.gp_log);
+    na.gp_log = na.gp_tick + kGpMaxLaunches;
+  }
   const bool fused = ns_final_fused(iters, x3);
   if (fused) {
     // the last update's epilogue writes W (or the output) from its fp32 result
@@ -592,6 +602,13 @@ muon_status_t muon_check_wait_timeout(void* workspace, size_t workspace_bytes,
   if (cudaMemsetAsync(workspace, 0, kHeaderBytes, st) != cudaSuccess) return MUON_ERR_CUDA;
   return cuda_status(
       launch_wait_timeout_check(static_cast<uint32_t*>(workspace), timeout_ns, st));
+}
+
+muon_status_t muon_occupy_sms(int blocks, size_t smem_bytes, uint64_t ns, muon_stream_t stream) {
+  if (blocks < 1 || blocks > 4096 || smem_bytes > (size_t{227} << 10) || ns == 0 ||
+      ns > 1000000000ull)
+    return MUON_ERR_INVALID_ARG;
+  return cuda_status(launch_occupy(blocks, smem_bytes, ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 muon_status_t muon_adamw_step(const muon_adamw_group_t* groups, int n_groups,

@@ -1163,28 +1163,188 @@ __global__ void __launch_bounds__(256) k_gram_reduce(const GramReduceArgs a) {
   }
 }
 
+// ---- split-K Gram of a 128 x 128 S with the polynomial, on CUDA cores -----
+// For Grams of at most 128 rows over a long K (the per-head matrices of a
+// split_head weight), the K-slices' fp32 sums are added in index order into
+// S in shared memory (fp32, scaled by 1/||X||^2 on the first iteration) and
+// P = b S + c S^2 + (a - 1) I is formed there directly, in fp32, and stored
+// in bf16 with its diagonal's rounding residual: one pass instead of a
+// reduction pass, a bf16 S and a 128 x 128 x 128 tensor-core launch whose
+// time is all launch latency.  S^2 uses S's symmetry,
+// (S^2)_ij = sum_k S_ki S_kj, so that both operands are rows of S.  Each
+// block forms kRpRows rows of P of one matrix (k ascending: the result
+// depends on the matrix alone).
+constexpr int kRpN = 128;
+constexpr int kRpRows = 32;
+constexpr int kRpThreads = 256;  // (kRpRows / 4) x (kRpN / 4): a 4 x 4 block of P each
+constexpr size_t kRpSmem = static_cast<size_t>(kRpN) * kRpN * 4;
+
+struct GramReducePolyArgs {
+  const float* partial;   // [ksplit][batch][128][128] raw accumulators
+  int ksplit, batch;
+  __nv_bfloat16* P;       // [batch][128][128]
+  float* pdiag;           // [batch][128]
+  const float* mscale;    // [batch] (first iteration: 1/||X||) or nullptr
+  float cb, cc, cd;       // P = cb S + cc S^2 + cd I
+};
+
+__global__ void __launch_bounds__(kRpThreads) k_gram_reduce_poly(const GramReducePolyArgs a) {
+  extern __shared__ __align__(16) float Ssm[];  // [128][128]
+  griddep_wait();
+  const int b = blockIdx.y, r0 = blockIdx.x * kRpRows, tid = threadIdx.x;
+  const float ms = a.mscale != nullptr ? a.mscale[b] : 1.f;
+  const float f = ms * ms;
+  constexpr int kPer = kRpN * kRpN / 4 / kRpThreads;  // float4 of S per thread
+  const int64_t mat = static_cast<int64_t>(kRpN) * kRpN;
+  // all of a thread's loads of two slices in flight at once (the sums are
+  // latency-bound otherwise); slices added in index order
+  float4 sum[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sl = 0; sl < a.ksplit; sl += 2) {
+    const float4* s0 = reinterpret_cast<const float4*>(
+        a.partial + (static_cast<int64_t>(sl) * a.batch + b) * mat);
+    const float4* s1 = reinterpret_cast<const float4*>(
+        a.partial + (static_cast<int64_t>(sl + 1) * a.batch + b) * mat);
+    const bool two = sl + 1 < a.ksplit;
+    float4 x[kPer], y[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      x[i] = __ldcg(s0 + tid + i * kRpThreads);
+      y[i] = two ? __ldcg(s1 + tid + i * kRpThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      sum[i].x += x[i].x; sum[i].y += x[i].y; sum[i].z += x[i].z; sum[i].w += x[i].w;
+      if (two) {
+        sum[i].x += y[i].x; sum[i].y += y[i].y; sum[i].z += y[i].z; sum[i].w += y[i].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    reinterpret_cast<float4*>(Ssm)[tid + i * kRpThreads] =
+        make_float4(sum[i].x * f, sum[i].y * f, sum[i].z * f, sum[i].w * f);
+  __syncthreads();
+  const int i0 = r0 + 4 * (tid >> 5), j0 = 4 * (tid & 31);
+  float acc[4][4] = {};
+#pragma unroll 4
+  for (int k = 0; k < kRpN; ++k) {
+    const float4 x = *reinterpret_cast<const float4*>(Ssm + k * kRpN + i0);  // S_ki (warp-uniform)
+    const float4 y = *reinterpret_cast<const float4*>(Ssm + k * kRpN + j0);  // S_kj
+    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = fmaf(xs[ii], ys[jj], acc[ii][jj]);
+  }
+  __nv_bfloat16* P = a.P + static_cast<int64_t>(b) * mat;
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = i0 + ii;
+    const float4 sv = *reinterpret_cast<const float4*>(Ssm + i * kRpN + j0);
+    float v[4] = {fmaf(a.cc, acc[ii][0], a.cb * sv.x), fmaf(a.cc, acc[ii][1], a.cb * sv.y),
+                  fmaf(a.cc, acc[ii][2], a.cb * sv.z), fmaf(a.cc, acc[ii][3], a.cb * sv.w)};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      if (i == j0 + jj) {
+        v[jj] += a.cd;
+        a.pdiag[static_cast<int64_t>(b) * kRpN + i] =
+            v[jj] - __bfloat162float(__float2bfloat16_rn(v[jj]));
+      }
+    uint2 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+    h[0] = __floats2bfloat162_rn(v[0], v[1]);
+    h[1] = __floats2bfloat162_rn(v[2], v[3]);
+    *reinterpret_cast<uint2*>(P + static_cast<int64_t>(i) * kRpN + j0) = u;
+  }
+}
+
 // Gram and polynomial of one iteration in one launch of the pair-wide
-// kernel (bf16 precision, c != 0): each CTA pair takes its Gram units, then
-// its polynomial units, with one pipeline state across both, so that its
-// producer loads polynomial operands while the epilogues drain the last Gram
-// tiles and the Gram's partly filled last round of tiles costs nothing.  A
-// polynomial unit of matrix b reads S_b, written by all of b's Gram units:
-// every epilogue warp adds 1 to the matrix's arrival counter once its TMA
-// stores of a Gram unit are complete (counted at the start of its next unit,
-// before that unit's accumulator wait, never after it), and the polynomial's
-// producer and epilogue wait (bounded) until the counter reaches the launch's
-// target.  Both phases walk the batch forward, so the first polynomial units
-// read matrices whose Gram finished about a round of tiles per matrix
-// earlier; the counters are cumulative over a call's launches (zeroed by
-// k_finalize_norm).
+// kernel (bf16 precision, c != 0).  The launch's work units are numbered by
+// tickets: every Gram unit (matrix-major) before any polynomial unit.  Each
+// CTA pair claims its next ticket from a per-launch counter (one atomic
+// add by the even CTA's producer, one unit ahead of the one it loads) and
+// records it in its row of a ticket log in global memory, stamped with the
+// launch's number; the odd CTA's producer and both CTAs' epilogue warps read
+// their units from that row, and the MMA issuer from a per-stage tag the
+// producer writes next to the operand stage (ticket_unit gives the order of
+// the units).  A polynomial unit of matrix b
+// reads S_b, written by all of b's Gram units: every epilogue warp adds 1 to
+// the matrix's arrival counter once its TMA stores of a Gram unit are
+// complete (counted at the start of its next unit, before that unit's
+// accumulator wait, never after it), and the polynomial's producer and
+// epilogue wait (bounded) until the counter reaches the launch's target.
+// Because a ticket is only ever held by a CTA pair that is running, and every
+// Gram ticket of a matrix is handed out before its first polynomial ticket,
+// every Gram unit a polynomial unit waits for belongs to a resident pair that
+// finishes it without waiting on anything (a pair's Gram units precede its
+// polynomial units of the same matrices): the launch makes progress however
+// few of its clusters the GPU runs at a time (other work may hold SMs).
+// On a diagonal super-block each CTA's half of B is its own A rows: the
+// operand is loaded once and the MMA reads it as both.  The
+// counters are cumulative over a call's launches (zeroed by k_finalize_norm);
+// the ticket counters and log are zeroed once per chain.
 constexpr int kArrivalsPerUnit = 2 * kEpiWarps2;  // epilogue warps of a CTA pair
+constexpr int kTicketDone = 0xFFFFFF;             // log entry: no further unit
+constexpr int kTicketMask = 0xFFFFFF;
+constexpr int kTagDone = -1;                      // stage tag: no further unit
 
 struct GramPolyParams {
   GemmParams g;   // Gram phase
   GemmParams q;   // polynomial phase
   int* ctr;       // [batch] Gram arrivals, cumulative over the call's launches
   int target;     // counter value at which this launch's Gram of a matrix is complete
+  int* tick;      // this launch's ticket counter (zero on entry)
+  int* log;       // [clusters][log_cap] tickets claimed by each CTA pair, as stamp | (ticket + 1)
+  int log_cap;    // entries per pair (>= all tickets + 2)
+  int stamp;      // this launch's number within the chain, << 24
+  int blk;        // matrices per ticket block
 };
+
+// Ticket -> phase (0 Gram, 1 polynomial) and unit index within the phase.
+// Tickets run in blocks of `blk` matrices, each block's polynomial units one
+// block behind its Gram units:
+//   [G_0] [G_1 P_0] [G_2 P_1] ... [G_last P_last-1] [P_last]
+// so that every Gram ticket of a matrix precedes its polynomial tickets (the
+// hand-over's progress needs that) and S is read back about one block after
+// it is written, while it is still in L2.  Units within a phase are
+// matrix-major, as decode_unit takes them.
+__device__ __forceinline__ void ticket_unit(const GramPolyParams& P, int T, int& ph, int& t) {
+  const int total = P.g.total_tiles;                 // units per phase
+  const int F = P.blk * P.g.tiles_per_matrix;        // units of a full block
+  const int nb = (total + F - 1) / F;
+  if (nb <= 1) {
+    ph = T >= total ? 1 : 0;
+    t = ph ? T - total : T;
+    return;
+  }
+  if (T < F) {
+    ph = 0;
+    t = T;
+    return;
+  }
+  T -= F;
+  const int q = T / (2 * F);
+  if (q < nb - 2) {  // the pair (G_{q+1}, P_q)
+    const int r = T - q * 2 * F;
+    ph = r < F ? 0 : 1;
+    t = r < F ? (q + 1) * F + r : q * F + (r - F);
+    return;
+  }
+  T -= (nb - 2) * 2 * F;
+  const int last = total - (nb - 1) * F;  // units of the last block
+  if (T < last) {
+    ph = 0;
+    t = (nb - 1) * F + T;
+  } else if (T < last + F) {
+    ph = 1;
+    t = (nb - 2) * F + (T - last);
+  } else {
+    ph = 1;
+    t = (nb - 1) * F + (T - last - F);
+  }
+}
 
 __global__ void __launch_bounds__(kGemmThreads2, 1)
     k_ns_gram_poly(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
@@ -1206,16 +1366,21 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
   uint64_t* tfull = empty + kStages2;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* first_bar = drain + 1;  // odd CTA: its first ticket has arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(first_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // even CTA: for the stage holding a unit's first k-block, the unit's
+  // k-blocks << 1 | whether it is diagonal (or kTagDone)
+  volatile int* unit_tag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* first_tick = reinterpret_cast<volatile int*>(tmem_slot + 2 + kStages2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = (rank == 0);
-  const int unit0 = static_cast<int>(blockIdx.x >> 1);
-  const int ustep = static_cast<int>(gridDim.x >> 1);
   uint32_t* const status = P.g.status;
   const uint64_t timeout_ns = P.g.timeout_ns;
+  const int n_tickets = P.g.total_tiles + P.q.total_tiles;
+  int* const my_log = P.log + static_cast<int64_t>(blockIdx.x >> 1) * P.log_cap;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages2; ++s) {
@@ -1227,6 +1392,7 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
       mbar_init(&tempty[a], 2 * kEpiWarps2);
     }
     mbar_init(drain, 1);
+    mbar_init(first_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -1243,7 +1409,31 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (threadIdx.x == 0) griddep_launch_dependents();
+  // The even CTA claims tickets two units ahead of the one it loads and logs
+  // them.  Its first two claims are made before the wait for the previous
+  // kernel (they touch only this launch's own counter), and the first goes
+  // to the odd CTA's shared memory directly; the log is written only after
+  // the wait, since the fused launch before the previous kernel may still be
+  // reading its rows until then.  The odd CTA reads its later units from the
+  // log, each written a whole unit before it is needed.
+  auto enc = [&](int t) { return P.stamp | (t >= n_tickets ? kTicketDone : t + 1); };
+  auto dec = [](int e) { return (e & kTicketMask) == kTicketDone ? kTicketDone : (e & kTicketMask) - 1; };
+  int T = kTicketDone, nxt = kTicketDone;
+  if (warp == 0 && lane == 0 && leader) {
+    T = atomicAdd(P.tick, 1);
+    if (T >= n_tickets) T = kTicketDone;
+    st_shared_cluster(mapa_shared(const_cast<int*>(first_tick), 1), T);
+    mbar_arrive_release_cluster(mapa_shared(first_bar, 1));
+    if (T != kTicketDone) {
+      nxt = atomicAdd(P.tick, 1);
+      if (nxt >= n_tickets) nxt = kTicketDone;
+    }
+  }
   griddep_wait();  // the previous kernel's outputs are this kernel's inputs
+  if (warp == 0 && lane == 0 && leader) {
+    st_relaxed_gpu(my_log, enc(T));
+    if (T != kTicketDone) st_relaxed_gpu(my_log + 1, enc(nxt));
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1252,38 +1442,81 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int ph = 0; ok && ph < 2; ++ph) {
+      if (!leader) {
+        ok = mbar_wait_acquire_cluster(first_bar, 0, abort_flag, status, timeout_ns);
+        T = *first_tick;
+      }
+      for (int j = 0; ok; ++j) {
+        if (T == kTicketDone) {
+          if (leader) {
+            // tell the MMA issuer there is no further unit
+            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status, timeout_ns))
+              break;
+            unit_tag[stage] = kTagDone;
+            mbar_arrive(&full[stage]);
+            // the drain below waits for this (at once complete) phase of the
+            // stage, not for the one before it
+            issued |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          }
+          break;
+        }
+        int ph, t;
+        ticket_unit(P, T, ph, t);
         const GemmParams& p = ph ? P.q : P.g;
         const CUtensorMap* tm_ab = ph ? &tmS : &tmX;
         const int nkb = p.K / kBK;
-        for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
-          int b, tm, tn;
-          decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
-          if (ph) {
-            // S_b complete (normally long since)
-            if (!wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns)) {
-              ok = false;
-              break;
-            }
-            fence_proxy_async_global();  // the TMA loads below read what the acquire saw
+        int b, tm, tn;
+        decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
+        const bool diag = (tm >> 1) == tn;  // B's rows of this CTA = its A rows
+        if (ph) {
+          // S_b complete (normally long since)
+          if (!wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns)) {
+            ok = false;
+            break;
           }
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status, timeout_ns)) {
-              ok = false;
-              break;
-            }
-            const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
-            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes2);
-            tma_load_3d_pair(smA + stage * kHalfBytes2, tm_ab, bar, kb * kBK, tm * kBM, b);
+          fence_proxy_async_global();  // the TMA loads below read what the acquire saw
+        }
+        // even CTA: the unit after next, claimed now (its atomic completes
+        // while this unit's k-blocks are issued) and logged with the last one
+        int nn = kTicketDone;
+        if (leader && nxt != kTicketDone && j + 2 < P.log_cap) nn = atomicAdd(P.tick, 1);
+        int peek = 0;  // odd CTA: the log entry of the next unit, loaded ahead
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, status, timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = full0 + static_cast<uint32_t>(stage) * 8u;
+          if (leader) {
+            if (kb == 0) unit_tag[stage] = (nkb << 1) | (diag ? 1 : 0);
+            mbar_arrive_expect_tx(&full[stage], diag ? 2 * kHalfBytes2 : 2 * kStageBytes2);
+          }
+          tma_load_3d_pair(smA + stage * kHalfBytes2, tm_ab, bar, kb * kBK, tm * kBM, b);
+          if (!diag)
             tma_load_3d_pair(smB + stage * kHalfBytes2, tm_ab, bar, kb * kBK,
                              tn * BN + static_cast<int>(rank) * 128, b);
-            issued |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages2) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          if (!leader && kb == 0) peek = ld_relaxed_gpu(my_log + j + 1);
+          if (leader && kb == nkb - 1 && nxt != kTicketDone && j + 2 < P.log_cap) {
+            if (nn >= n_tickets) nn = kTicketDone;
+            st_relaxed_gpu(my_log + j + 2, enc(nn));
           }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (leader) {
+          T = nxt;
+          nxt = nn;
+        } else {
+          if ((peek & ~kTicketMask) != P.stamp &&
+              !wait_stamped_bounded(my_log + j + 1, P.stamp, &peek, abort_flag, status, timeout_ns))
+            break;
+          T = dec(peek);
         }
       }
       if (leader)
@@ -1296,41 +1529,43 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
       // ---------------------------------------------------------- MMA issuer
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int ph = 0; ok && ph < 2; ++ph) {
-        const GemmParams& p = ph ? P.q : P.g;
-        const int nkb = p.K / kBK;
-        for (int t = unit0; ok && t < p.total_tiles; t += ustep) {
-          if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status, timeout_ns))
+      while (true) {
+        // the unit's first stage carries its length and kind
+        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, status, timeout_ns)) break;
+        const int tag = unit_tag[stage];
+        if (tag == kTagDone) break;
+        const int nkb = tag >> 1;
+        const bool diag = (tag & 1) != 0;
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort_flag, status, timeout_ns))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (kb > 0 && !mbar_wait_bounded(&full[stage], phase, abort_flag, status, timeout_ns)) {
+            ok = false;
             break;
+          }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-          for (int kb = 0; kb < nkb; ++kb) {
-            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, status, timeout_ns)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t a_addr = smem_u32(smA + stage * kHalfBytes2);
-            const uint32_t b_addr = smem_u32(smB + stage * kHalfBytes2);
+          const uint32_t a_addr = smem_u32(smA + stage * kHalfBytes2);
+          const uint32_t b_addr = diag ? a_addr : smem_u32(smB + stage * kHalfBytes2);
 #pragma unroll
-            for (int ks = 0; ks < kBK / 16; ++ks) {
-              const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(b_addr + ks * 32, 16, 1024);
-              tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
-            }
-            tc_commit_pair_multicast(&empty[stage], 0x3);
-            if (++stage == kStages2) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            const uint64_t ad = smem_desc_sw128(a_addr + ks * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          if (!ok) break;
-          tc_commit_pair_multicast(&tfull[acc], 0x3);
-          if (++acc == kAccBufs2) {
-            acc = 0;
-            acc_phase ^= 1u;
+          tc_commit_pair_multicast(&empty[stage], 0x3);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1u;
           }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(&tfull[acc], 0x3);
+        if (++acc == kAccBufs2) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
       }
       tc_commit_pair_multicast(drain, 0x1);
@@ -1346,53 +1581,54 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int pending = -1;  // matrix of the last Gram unit whose arrival is not yet counted
-    bool ok = true;
-    for (int ph = 0; ok && ph < 2; ++ph) {
-      const GemmParams& p = ph ? P.q : P.g;
-      for (int t = unit0; t < p.total_tiles; t += ustep) {
-        if (pending >= 0) {
-          if (lane == 0) {
-            tma_store_wait_all0();
-            fence_proxy_async_global();
-            red_release_gpu_add(P.ctr + pending, 1);
-          }
-          pending = -1;
+    int peek = lane == 0 ? ld_relaxed_gpu(my_log) : 0;  // log entry of the next unit
+    for (int j = 0;; ++j) {
+      int e = peek, ok = 1;
+      if (lane == 0 && (e & ~kTicketMask) != P.stamp)
+        ok = wait_stamped_bounded(my_log + j, P.stamp, &e, abort_flag, status, timeout_ns);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      e = __shfl_sync(0xffffffffu, e, 0);
+      if (!ok || (e & kTicketMask) == kTicketDone) break;
+      if (lane == 0 && j + 1 < P.log_cap) peek = ld_relaxed_gpu(my_log + j + 1);
+      if (pending >= 0) {
+        if (lane == 0) {
+          tma_store_wait_all0();
+          fence_proxy_async_global();
+          red_release_gpu_add(P.ctr + pending, 1);
         }
-        int b, tm, tn;
-        decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
-        bool r;
-        if (ph == 0) {
-          r = epilogue_tile<BN, kEpiGram, true, kChunks, true>(
-              p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
-              acc_phase, abort_flag, c_begin, &tmSo, &tmSo, sbuf);
-        } else {
-          // the epilogue reads S_b itself (b S term): wait for it here too
-          int ready = 1;
-          if (lane == 0)
-            ready = wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns);
-          ready = __shfl_sync(0xffffffffu, ready, 0);
-          if (!ready) {
-            ok = false;
-            break;
-          }
-          __syncwarp();  // lane 0's acquire orders every lane's reads of S_b
-          r = epilogue_tile<BN, kEpiPoly, true, kChunks, true>(
-              p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
-              acc_phase, abort_flag, c_begin, &tmPo, &tmPo, sbuf);
-        }
-        if (!r) {
-          ok = false;
-          break;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
-        if (++acc == kAccBufs2) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-        if (ph == 0) pending = b;
+        pending = -1;
       }
+      int ph, t;
+      ticket_unit(P, (e & kTicketMask) - 1, ph, t);
+      const GemmParams& p = ph ? P.q : P.g;
+      int b, tm, tn;
+      decode_unit<BN, true, true>(p, t, rank, b, tm, tn);
+      bool r;
+      if (ph == 0) {
+        r = epilogue_tile<BN, kEpiGram, true, kChunks, true>(
+            p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
+            acc_phase, abort_flag, c_begin, &tmSo, &tmSo, sbuf);
+      } else {
+        // the epilogue reads S_b itself (b S term): wait for it here too
+        int ready = 1;
+        if (lane == 0)
+          ready = wait_counter_bounded(P.ctr + b, P.target, abort_flag, status, timeout_ns);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) break;
+        __syncwarp();  // lane 0's acquire orders every lane's reads of S_b
+        r = epilogue_tile<BN, kEpiPoly, true, kChunks, true>(
+            p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
+            acc_phase, abort_flag, c_begin, &tmPo, &tmPo, sbuf);
+      }
+      if (!r) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      if (++acc == kAccBufs2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+      if (ph == 0) pending = b;
     }
     if (lane == 0) {
       tma_store_wait_all0();
@@ -1580,8 +1816,10 @@ cudaError_t launch_gram_poly(const CUtensorMap& x, const CUtensorMap& sk, const 
   e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters < 1) return cudaErrorInvalidConfiguration;
-  // every cluster resident at once: polynomial units wait on other clusters' Gram units
-  const int units = std::max(1, std::min(gp.g.total_tiles, clusters));
+  // at most one pair per Gram unit (more would only claim polynomial units
+  // early and wait) and per row of the ticket log; the ticket hand-over needs
+  // no pair to be resident alongside any other
+  const int units = std::max(1, std::min(std::min(gp.g.total_tiles, clusters), kGpMaxClusters));
   cfg.gridDim = dim3(2 * units);
   if (kUsePdl) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1658,6 +1896,13 @@ int gram_ksplit(int n_pad, int m_pad, bool x3) {
 }
 
 bool ns_final_has_lo(int iters, bool x3) { return x3 || iters < kLoIters; }
+
+size_t gram_poly_log_ints(int batch, int n_pad, bool x3) {
+  if (x3 || n_pad % 256 != 0) return 0;
+  const int64_t S = n_pad / 256;
+  const int64_t tickets = 2 * static_cast<int64_t>(batch) * (S * (S + 1) / 2);
+  return static_cast<size_t>(kGpMaxLaunches + kGpMaxClusters * (tickets + 2));
+}
 
 cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   if (a.iters == 0) return cudaSuccess;
@@ -1742,8 +1987,9 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
     q.mscale = nullptr;
     if (x3) q.lo_in = 1;
     // Gram and polynomial in one launch where both run on CTA pairs (bf16)
-    const bool gp_fuse = kFuseGramPoly && !x3 && pair && bn_sq == 256 &&
-                         cc != 0.f && a.gp_ctr != nullptr && ksplit == 1;
+    const bool gp_fuse = kFuseGramPoly && !x3 && pair && bn_sq == 256 && cc != 0.f &&
+                         a.gp_ctr != nullptr && a.gp_log != nullptr && ksplit == 1 &&
+                         gp_launches < kGpMaxLaunches;
     if (gp_fuse) {
       GramPolyParams gp{};
       gp.g = g;
@@ -1751,10 +1997,56 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       gp.g.reverse = 0;  // both phases walk forward (the polynomial trails the Gram)
       gp.q.reverse = 0;
       gp.ctr = a.gp_ctr;
+      gp.tick = a.gp_tick + gp_launches;
+      gp.log = a.gp_log;
+      gp.log_cap = g.total_tiles + q.total_tiles + 2;
+      gp.stamp = (gp_launches + 1) << 24;
+      // a ticket block spans at least a round of tiles on every SM pair
+      gp.blk = std::max(1, (sm_count() / 2 + g.tiles_per_matrix - 1) / g.tiles_per_matrix);
       gp.target = (++gp_launches) * g.tiles_per_matrix * kArrivalsPerUnit;
       e = launch_gram_poly(X[cur].k128, S.k128, S.st, P.st, gp, f_gram + f_poly, st);
       if (e != cudaSuccess) return e;
       launch = 0;  // the update walks backwards, from the matrices the polynomial ended on
+    } else if (ksplit > 1 && cc != 0.f && batch <= 65535) {
+      // split-K: raw slice sums into the partial buffer, then S and P in one
+      // CUDA-core pass
+      GemmParams gs = g;
+      gs.ksplit = ksplit;
+      gs.partial = a.partial;
+      gs.total_tiles = g.total_tiles * ksplit;
+      gs.reverse = 0;
+      e = launch_sym<kEpiGram>(bn_sq, pair, X[cur], S, gs, f_gram, st);
+      if (e != cudaSuccess) return e;
+      GramReducePolyArgs ra{};
+      ra.partial = a.partial;
+      ra.ksplit = ksplit;
+      ra.batch = batch;
+      ra.P = a.B;
+      ra.pdiag = a.pdiag;
+      ra.mscale = g.mscale;
+      ra.cb = cb;
+      ra.cc = cc;
+      ra.cd = ca - 1.f;
+      e = cudaFuncSetAttribute(k_gram_reduce_poly, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kRpSmem));
+      if (e != cudaSuccess) return e;
+      cudaLaunchConfig_t rc = {};
+      cudaLaunchAttribute rattr[1];
+      rc.blockDim = dim3(kRpThreads);
+      rc.gridDim = dim3(kRpN / kRpRows, static_cast<unsigned>(batch));
+      rc.dynamicSmemBytes = kRpSmem;
+      rc.stream = st;
+      if (kUsePdl) {
+        rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        rattr[0].val.programmaticStreamSerializationAllowed = 1;
+        rc.attrs = rattr;
+        rc.numAttrs = 1;
+      }
+      prof_begin(kKindPoly, st);
+      e = cudaLaunchKernelEx(&rc, k_gram_reduce_poly, ra);
+      prof_end(kKindPoly, st, f_poly, 0.0);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
     } else if (ksplit > 1) {
       // split-K: raw slice sums into the partial buffer, then k_gram_reduce
       GemmParams gs = g;
@@ -1800,7 +2092,7 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       if (e != cudaSuccess) return e;
     }
 
-    if (cc != 0.f && !gp_fuse) {
+    if (cc != 0.f && !gp_fuse && (ksplit == 1 || batch > 65535)) {
       q.reverse = (launch++ & 1) == 0;
       e = x3 ? launch_sym<kEpiPoly | kEpiX3>(bn_sq, pair, S, P, q, f_poly, st)
              : launch_sym<kEpiPoly>(bn_sq, pair, S, P, q, f_poly, st);

@@ -122,6 +122,46 @@ __device__ __forceinline__ bool wait_counter_bounded(const int* ctr, int target,
   }
 }
 
+// Relaxed gpu-scope load / store of a word that carries no other data with it
+// (a claimed work-unit number).
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(int* p, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait (bounded) until the word at p carries `stamp` in its top byte (bits
+// 24..31); returns the word through *out.  On timeout: sets the abort flag
+// and MUON_FLAG_TIMEOUT, returns false.
+__device__ __forceinline__ bool wait_stamped_bounded(const int* p, int stamp, int* out,
+                                                     volatile int* abort, uint32_t* status,
+                                                     uint64_t timeout_ns) {
+  int v = ld_relaxed_gpu(p);
+  if ((v & ~0xFFFFFF) == stamp) {
+    *out = v;
+    return true;
+  }
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(32);
+    v = ld_relaxed_gpu(p);
+    if ((v & ~0xFFFFFF) == stamp) {
+      *out = v;
+      return true;
+    }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicOr(status, 0x2u /* MUON_FLAG_TIMEOUT */);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) — 3-D tiled loads into shared memory
 // ---------------------------------------------------------------------------
@@ -229,6 +269,44 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
 // global store of the thread to be acknowledged) is not needed.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
+// Hand a word to the same shared variable of another CTA of the cluster:
+// store it there, then arrive on that CTA's mbarrier with cluster-scope
+// release, so that a cluster-scope acquire wait on the barrier sees the word.
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+               : "memory");
+}
+
+// Bounded wait, with cluster-scope acquire, for the phase of this CTA's
+// mbarrier `bar` with the given parity (a word handed over by another CTA).
+__device__ __forceinline__ bool mbar_wait_acquire_cluster(uint64_t* bar, uint32_t parity,
+                                                          volatile int* abort, uint32_t* status,
+                                                          uint64_t timeout_ns) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicOr(status, 0x2u /* MUON_FLAG_TIMEOUT */);
+      return false;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

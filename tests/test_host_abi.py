@@ -182,11 +182,16 @@ def oracle_hybrid():
 
 
 def test_split_bf16_workspace_adds_lo_planes_of_s_and_p(lib):
+    """The split-bf16 layout adds lo planes of S and P, and drops the ticket
+    counters and log of the fused bf16 Gram + polynomial launches (64
+    counters, then 128 rows of one launch's tickets + 2: 2 x 64 matrices x
+    10 upper 256 x 256 super-blocks of a 1024^2 Gram)."""
     x3 = m.Schedule([(1, (1.0, 0.0, 0.0))], prec=m.MUON_NS_BF16X3)
     code, nb = _ws_size([_group(1024, 1024, batch=64)])
     code3, nb3 = _ws_size([_group(1024, 1024, batch=64)], x3.ref)
     assert code == code3 == m.MUON_OK
-    assert nb3 == nb + 2 * 64 * 1024 * 1024 * 2
+    log_bytes = (64 + 128 * (2 * 64 * 10 + 2)) * 4
+    assert nb3 == nb + 2 * 64 * 1024 * 1024 * 2 - (log_bytes + 255) // 256 * 256
 
 
 def test_schedule_validation(lib):
@@ -290,3 +295,11 @@ def test_binding_fails_loudly_without_library(tmp_path):
             m.load_library(str(tmp_path / "missing.so"))
     finally:
         m._lib = saved
+
+
+def test_occupy_sms_rejects_out_of_range_arguments(lib):
+    L = m.load_library()
+    assert L.muon_occupy_sms(0, 1024, 1000, None) == m.MUON_ERR_INVALID_ARG
+    assert L.muon_occupy_sms(4, 228 << 10, 1000, None) == m.MUON_ERR_INVALID_ARG
+    assert L.muon_occupy_sms(4, 1024, 0, None) == m.MUON_ERR_INVALID_ARG
+    assert L.muon_occupy_sms(4, 1024, 2_000_000_000, None) == m.MUON_ERR_INVALID_ARG
