@@ -114,9 +114,13 @@ constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, 4 epilogue 
 // kEpiX3 (or-ed into Gram / Poly / Update): the split-bf16 precision, in
 // which S, P and X are all stored as hi + lo planes and every product is the
 // three-term sum A_hi B_hi + A_hi B_lo + A_lo B_hi.
-enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2, kEpiFinal = 3, kEpiX3 = 4 };
+// kEpiTall (or-ed into kEpiFinal): some matrix of the chain keeps W (or its
+// output) in the tall orientation, so the epilogue carries the turn-around
+// path and its shared-memory buffers; without it the kernel serves wide W only.
+enum Epi : int { kEpiGram = 0, kEpiPoly = 1, kEpiUpdate = 2, kEpiFinal = 3, kEpiX3 = 4, kEpiTall = 8 };
 __host__ __device__ constexpr int epi_kind(int e) { return e & 3; }
 __host__ __device__ constexpr bool epi_x3(int e) { return (e & kEpiX3) != 0; }
+__host__ __device__ constexpr bool epi_tall(int e) { return (e & kEpiTall) != 0; }
 
 template <int BN>
 struct Cfg {
@@ -324,11 +328,13 @@ __device__ __forceinline__ void fin_prefetch(const FinalStore& f, const FinTile&
 }
 
 // W of one chunk into registers (raw bits; bf16 wide packs two per word).
-__device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, int row, int col0,
-                                         uint32_t (&w)[32]) {
-  if (t.base == nullptr || f.mode != 1 || row >= t.n_real) return;
+template <bool kTall>
+__device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, int row, int row0,
+                                         int col0, uint32_t (&w)[32]) {
+  if (t.base == nullptr || f.mode != 1) return;
   const bool bf = t.bf;
-  if (!t.tall) {
+  if (!kTall || !t.tall) {
+    if (row >= t.n_real) return;
     // whole 32-byte sectors where the row allows (m_real is a multiple of 8)
     const int64_t roff = static_cast<int64_t>(row) * t.ld;
     if (t.v8 && col0 + 32 <= t.m_real) {
@@ -367,25 +373,122 @@ __device__ __forceinline__ void fin_load(const FinalStore& f, const FinTile& t, 
       }
     }
   } else {
+    // turned-around layout (see fin_store): half h of the chunk gives this
+    // lane 16 consecutive elements of W row col0 + 16h + lane / 2, from
+    // wide row row0 + 16 (lane & 1); bf16 packs two per word (words 8h..8h+7),
+    // fp32 one (words 16h..16h+15)
+    const int lane = row - row0;
+    const int i0 = row0 + 16 * (lane & 1);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int j = col0 + e;
+    for (int h = 0; h < 2; ++h) {
+      const int j = col0 + 16 * h + (lane >> 1);
       if (j >= t.m_real) continue;
-      const int64_t off = static_cast<int64_t>(j) * t.ld + row;
-      w[e] = bf ? static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(
-                      static_cast<const __nv_bfloat16*>(t.base) + off))
-                : *reinterpret_cast<const uint32_t*>(static_cast<const float*>(t.base) + off);
+      const int64_t off = static_cast<int64_t>(j) * t.ld + i0;
+      if (i0 + 16 <= t.n_real) {
+        if (bf) {
+          const uint4* q = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(t.base) + off);
+          const uint4 a = q[0], b = q[1];
+          w[8 * h] = a.x; w[8 * h + 1] = a.y; w[8 * h + 2] = a.z; w[8 * h + 3] = a.w;
+          w[8 * h + 4] = b.x; w[8 * h + 5] = b.y; w[8 * h + 6] = b.z; w[8 * h + 7] = b.w;
+        } else {
+          const uint4* q = reinterpret_cast<const uint4*>(static_cast<const float*>(t.base) + off);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 a = q[k];
+            w[16 * h + 4 * k] = a.x; w[16 * h + 4 * k + 1] = a.y;
+            w[16 * h + 4 * k + 2] = a.z; w[16 * h + 4 * k + 3] = a.w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          if (i0 + k >= t.n_real) continue;
+          if (bf) {
+            const uint32_t hb = *reinterpret_cast<const unsigned short*>(
+                static_cast<const __nv_bfloat16*>(t.base) + off + k);
+            w[8 * h + (k >> 1)] = (k & 1) ? ((w[8 * h + (k >> 1)] & 0xffffu) | (hb << 16))
+                                          : ((w[8 * h + (k >> 1)] & 0xffff0000u) | hb);
+          } else {
+            w[16 * h + k] = *reinterpret_cast<const uint32_t*>(static_cast<const float*>(t.base) + off + k);
+          }
+        }
+      }
     }
   }
 }
 
-__device__ __forceinline__ float fin_w(bool bf, bool tall, const uint32_t (&w)[32], int e) {
+// Element e of a lane's W words (bf16 packed two per word, or fp32).
+__device__ __forceinline__ float fin_w(bool bf, const uint32_t (&w)[32], int e) {
   if (!bf) return __uint_as_float(w[e]);
-  // bf16 bits: packed pairs (wide) or one per word (tall)
-  const uint32_t h = tall ? (w[e] & 0xffffu) : ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu));
+  const uint32_t h = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xffffu);
   return __uint_as_float(h << 16);
 }
 
+// Rows of a warp's buffer for turning a tall tile's chunk around: 16 chunk
+// columns x 32 wide rows, padded to 33 words (conflict-free both ways).
+constexpr int kTurnRows = 16;
+constexpr int kTurnLd = 33;
+constexpr uint32_t kTurnBytesPerWarp = kTurnRows * kTurnLd * 4;
+
+// Tall W (W[j][i] holds the wide element (i, j)): the warp's 32 x 32 block
+// of O' (lane = wide row row0 + lane, v[e] = wide column col0 + e) is turned
+// around through the warp's shared-memory buffer in two halves of 16 columns,
+// after which each lane holds 16 consecutive elements of one W row (row
+// col0 + 16h + lane / 2, from wide row row0 + 16 (lane & 1)) and reads,
+// updates and writes them with 16-byte accesses.  Warp-collective: every
+// lane of the warp calls it for the same tile.
+__device__ __forceinline__ void fin_store_tall(const FinalStore& f, const FinTile& t, int row0,
+                                               int col0, const float (&v)[32],
+                                               const uint32_t (&w)[32], float* turn, int lane) {
+  const bool muon = (f.mode == 1);
+  const bool bf = t.bf;
+  const int i0 = row0 + 16 * (lane & 1);
+  const float* src = turn + (lane >> 1) * kTurnLd + 16 * (lane & 1);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    __syncwarp();  // the previous half's reads are done
+#pragma unroll
+    for (int e = 0; e < 16; ++e) turn[e * kTurnLd + lane] = v[16 * h + e];
+    __syncwarp();
+    const int j = col0 + 16 * h + (lane >> 1);
+    if (t.base == nullptr || j >= t.m_real || i0 >= t.n_real) continue;
+    const int64_t off = static_cast<int64_t>(j) * t.ld + i0;
+    const bool whole = i0 + 16 <= t.n_real;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {  // 8 elements at a time
+      float o[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        o[k] = src[8 * g + k];
+        if (muon) o[k] = fmaf(-t.lr_scale, o[k], fin_w(bf, w, 16 * h + 8 * g + k) * t.decay);
+      }
+      if (whole) {
+        if (bf) {
+          uint4 u;
+          __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hp[e] = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(t.base) + off + 8 * g) = u;
+        } else {
+          float4* d = reinterpret_cast<float4*>(static_cast<float*>(t.base) + off + 8 * g);
+          d[0] = make_float4(o[0], o[1], o[2], o[3]);
+          d[1] = make_float4(o[4], o[5], o[6], o[7]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (i0 + 8 * g + k >= t.n_real) continue;
+          if (bf)
+            static_cast<__nv_bfloat16*>(t.base)[off + 8 * g + k] = __float2bfloat16_rn(o[k]);
+          else
+            static_cast<float*>(t.base)[off + 8 * g + k] = o[k];
+        }
+      }
+    }
+  }
+}
+
+// Wide W: the lane's 32 elements are consecutive in W row `row`.
 __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t, int row, int col0,
                                           const float (&v)[32], const uint32_t (&w)[32]) {
   if (t.base == nullptr || row >= t.n_real) return;
@@ -393,9 +496,8 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
   const bool bf = t.bf;
   float o[32];
 #pragma unroll
-  for (int e = 0; e < 32; ++e)
-    o[e] = muon ? fmaf(-t.lr_scale, v[e], fin_w(bf, t.tall, w, e) * t.decay) : v[e];
-  if (!t.tall) {
+  for (int e = 0; e < 32; ++e) o[e] = muon ? fmaf(-t.lr_scale, v[e], fin_w(bf, w, e) * t.decay) : v[e];
+  {
     const int64_t roff = static_cast<int64_t>(row) * t.ld;
     if (t.v8 && col0 + 32 <= t.m_real) {
       if (bf) {
@@ -438,18 +540,6 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
         q[1] = make_float4(o[8 * k + 4], o[8 * k + 5], o[8 * k + 6], o[8 * k + 7]);
       }
     }
-  } else {
-    // W[j][row]: the warp's 32 lanes store 32 consecutive elements of W row j
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int j = col0 + e;
-      if (j >= t.m_real) continue;
-      const int64_t off = static_cast<int64_t>(j) * t.ld + row;
-      if (bf)
-        static_cast<__nv_bfloat16*>(t.base)[off] = __float2bfloat16_rn(o[e]);
-      else
-        static_cast<float*>(t.base)[off] = o[e];
-    }
   }
 }
 
@@ -461,7 +551,9 @@ __device__ __forceinline__ void fin_store(const FinalStore& f, const FinTile& t,
 // tensor core for shared-memory bandwidth.)  With kTmaOut the direct
 // (untransposed) store goes through a per-warp 2 KB staging box per plane
 // (32 rows x 64 bytes, 64-byte swizzle) and one TMA store per box, so L2
-// sees whole 64-byte row segments instead of one request per lane.
+// sees whole 64-byte row segments instead of one request per lane.  The last
+// update's epilogue gets the warp's turn-around buffer (kTurnBytesPerWarp) in
+// sbuf instead, for tall W.
 // Returns false if the wait gave up.
 template <int BN, int EPI, bool SYM, int kChunksPerWarp = BN / 32, bool kTmaOut = false>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_acc, int b, int tm,
@@ -489,6 +581,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     if (lo_in) load_raw4(aux_row + p.lo_off + c_begin * 32, cur_l);
   }
   constexpr bool kFin = (K == kEpiFinal);
+  constexpr bool kTall = kFin && epi_tall(EPI);
   // symmetric kinds of the bf16 precision: the mirrored copy goes out as a
   // TMA store of a transposed box too
   constexpr bool kMirrorTma = kTmaOut && SYM && !kX3;
@@ -497,7 +590,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
   if (kFin) {
     ft = fin_tile(p.fin, b);
     fin_prefetch(p.fin, ft, row, row0, tn * BN + c_begin * 32, kChunksPerWarp * 32, lane);
-    fin_load(p.fin, ft, row, tn * BN + c_begin * 32, w_cur);
+    fin_load<kTall>(p.fin, ft, row, row0, tn * BN + c_begin * 32, w_cur);
   }
   // per-tile scalars, loaded before the accumulator wait so that their
   // latency hides behind it: the first iteration's 1/||X|| and, in the
@@ -518,7 +611,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
     if (K != kEpiGram && i + 1 < kChunksPerWarp) {
       load_raw4(aux_row + (c + 1) * 32, nxt_h);
       if (lo_in) load_raw4(aux_row + p.lo_off + (c + 1) * 32, nxt_l);
-      if (kFin) fin_load(p.fin, ft, row, tn * BN + (c + 1) * 32, w_nxt);
+      if (kFin) fin_load<kTall>(p.fin, ft, row, row0, tn * BN + (c + 1) * 32, w_nxt);
     }
     uint32_t r[32];
     tmem_ld_32x32b_x32(t_row + c * 32, r);
@@ -594,7 +687,10 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, uint32_t t_ac
         }
     }
     if (kFin) {
-      fin_store(p.fin, ft, row, col0, v, w_cur);
+      if (kTall && ft.tall)
+        fin_store_tall(p.fin, ft, row0, col0, v, w_cur, reinterpret_cast<float*>(sbuf), lane);
+      else
+        fin_store(p.fin, ft, row, col0, v, w_cur);
       if (i + 1 < kChunksPerWarp) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) cur_h[k] = nxt_h[k];
@@ -853,6 +949,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter of this warp
+    // the last update's turn-around buffer for tall W, after the barriers
+    uint8_t* turn = epi_tall(EPI)
+                        ? smem + kStages * C::kStageBytes + 256 + (warp - 2) * kTurnBytesPerWarp
+                        : nullptr;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit0; t < p.total_tiles; t += ustep) {
@@ -860,7 +960,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       decode_unit<BN, SYM, false>(p, t / nsplit, 0u, b, tm, tn);
       if (!epilogue_tile<BN, EPI, SYM>(p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn,
                                        q, lane, &tfull[acc], acc_phase, abort_flag, 0, nullptr,
-                                       nullptr, nullptr, t % nsplit))
+                                       nullptr, turn, t % nsplit))
         break;
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -902,8 +1002,12 @@ constexpr uint32_t kStageBytes2 = 2 * kHalfBytes2;   // A + B half, per CTA
 // TMA-store staging: per epilogue warp one 2 KB box for the hi plane and one
 // for the lo plane (every kind but the last update, which writes W itself)
 constexpr uint32_t kStagingPerWarp2 = 4096;
+// (the last update has no TMA stores; its warps get turn-around buffers)
+__host__ __device__ constexpr uint32_t staging_per_warp2(int epi) {
+  return epi_kind(epi) != kEpiFinal ? kStagingPerWarp2 : (epi_tall(epi) ? kTurnBytesPerWarp : 0u);
+}
 __host__ __device__ constexpr uint32_t staging_bytes2(int epi) {
-  return epi_kind(epi) == kEpiFinal ? 0u : kEpiWarps2 * kStagingPerWarp2;
+  return kEpiWarps2 * staging_per_warp2(epi);
 }
 __host__ __device__ constexpr size_t smem_bytes2(int epi) {
   return kStages2 * kStageBytes2 + staging_bytes2(epi) + 1024 + 256;
@@ -916,7 +1020,7 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
                const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmO2,
                const GemmParams p) {
   constexpr int BN = 256;
-  constexpr bool kTmaOut = staging_bytes2(EPI) != 0;
+  constexpr bool kTmaOut = epi_kind(EPI) != kEpiFinal;
   constexpr uint32_t kTmemCols = kAccBufs2 * BN;
   constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, BN, B_MN);
 
@@ -1078,7 +1182,7 @@ __global__ void __launch_bounds__(kGemmThreads2, 1)
       if (!epilogue_tile<BN, EPI, SYM, kChunksPerWarp2, kTmaOut>(
               p, tmem_base + static_cast<uint32_t>(acc * BN), b, tm, tn, q, lane, &tfull[acc],
               acc_phase, abort_flag, c_begin, &tmO, &tmO2,
-              staging + (warp - 2) * kStagingPerWarp2))
+              staging + (warp - 2) * staging_per_warp2(EPI)))
         break;
       tc_fence_before();
       __syncwarp();
@@ -1666,6 +1770,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+double l2_bytes() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0)
+    return 64.0 * (1 << 20);
+  return static_cast<double>(v);
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -1722,7 +1834,7 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, const CUt
                         const CUtensorMap& tb2, const GemmParams& p, double alg_flops,
                         cudaStream_t st) {
   auto kern = k_ns_gemm<BN, B_MN, EPI, SYM>;
-  const size_t smem = Cfg<BN>::kSmemBytes;
+  const size_t smem = Cfg<BN>::kSmemBytes + (epi_tall(EPI) ? kEpiWarps * kTurnBytesPerWarp : 0);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -2001,8 +2113,13 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       gp.log = a.gp_log;
       gp.log_cap = g.total_tiles + q.total_tiles + 2;
       gp.stamp = (gp_launches + 1) << 24;
-      // a ticket block spans at least a round of tiles on every SM pair
+      // a ticket block spans at least a round of tiles on every SM pair; the
+      // polynomial trails the Gram by a block only where a block's X and S
+      // fit in half of L2 (otherwise the two streams would evict each other:
+      // all Gram units first)
       gp.blk = std::max(1, (sm_count() / 2 + g.tiles_per_matrix - 1) / g.tiles_per_matrix);
+      const double block_bytes = static_cast<double>(gp.blk) * 2.0 * n * (static_cast<double>(m) + n);
+      if (block_bytes > 0.5 * l2_bytes()) gp.blk = batch;
       gp.target = (++gp_launches) * g.tiles_per_matrix * kArrivalsPerUnit;
       e = launch_gram_poly(X[cur].k128, S.k128, S.st, P.st, gp, f_gram + f_poly, st);
       if (e != cudaSuccess) return e;
@@ -2131,7 +2248,10 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
       u.fin = a.fin;
       u.lo_in = false;
       u.lo_out = false;
-      e = launch_upd<kEpiFinal>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
+      bool any_tall = false;
+      for (int k = 0; k < a.fin.nseg; ++k) any_tall = any_tall || a.fin.seg[k].tall != 0;
+      e = any_tall ? launch_upd<kEpiFinal | kEpiTall>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st)
+                   : launch_upd<kEpiFinal>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
     } else {
       e = launch_upd<kEpiUpdate>(bn_up, pair, P, X[cur], X[cur ^ 1], u, f_update, st);
     }
