@@ -405,7 +405,7 @@ def read_traffic(kernel: str, summary="ns_gemm_traffic_stack.json", files=("ns_g
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
     was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", summary)
-    if not os.path.exists(p):
+    if not summary or not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
@@ -620,7 +620,10 @@ def run_ours(args):
     d = timed[dom]
     avg_s = d["total_ms"] / d["launches"] / 1e3
     timing = f"event pair per launch, {prof_steps} profiled steps after the timed region"
-    traffic_file = f"ns_gemm_traffic_{args.workload}.json"
+    # the committed DRAM counters were taken in the default configuration
+    # (bf16 precision, one chain per group): other configurations report none
+    traffic_file = (f"ns_gemm_traffic_{args.workload}.json"
+                    if args.prec == "bf16" and not merge else "")
     if dom.startswith("ns_"):
         per_launch = d["alg_flops"] / d["launches"]
         achieved = per_launch / avg_s / 1e12
