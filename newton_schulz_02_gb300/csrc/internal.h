@@ -156,6 +156,7 @@ enum KernelKind : int {
   kKindTimeoutCheck,
   kKindAdamW,
   kKindGramPoly,
+  kKindChain,
   kKindCount
 };
 void prof_begin(KernelKind k, cudaStream_t st);

@@ -72,6 +72,7 @@
 // evaluated as written, X' = a X + (b S + c S^2) X.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -104,6 +105,12 @@ constexpr bool kUseTwoSm = MUON_TWO_SM != 0;  // pair-wide MMA (k_ns_gemm2) wher
 #endif
 // Gram and polynomial of an iteration in one launch (k_ns_gram_poly) where possible.
 constexpr bool kFuseGramPoly = MUON_FUSE_GRAM_POLY != 0;
+#ifndef MUON_CLUSTER_CHAIN
+#define MUON_CLUSTER_CHAIN 1
+#endif
+// Iterates of one 128-row tile run the whole chain in one launch
+// (k_ns_cluster_chain) where the GPU can hold its clusters.
+constexpr bool kUseClusterChain = MUON_CLUSTER_CHAIN != 0;
 constexpr int kBK = 64;   // k-block: 64 bf16 = one 128-byte swizzle row
 constexpr int kBandTiles = 8;  // update (non-symmetric, paired) tiles: column band width
 constexpr int kEpiWarps = 4;
@@ -1364,6 +1371,765 @@ __global__ void __launch_bounds__(kRpThreads) k_gram_reduce_poly(const GramReduc
   }
 }
 
+// ---- the whole chain on chip: iterates of one 128-row tile ------------------
+// For wide iterates of at most 128 rows (n <= 128: the per-head matrices of a
+// split_head weight, 128 x 4096, among them) the polynomial and the update
+// are short in K and the three-GEMM chain spends its time in launch latency
+// and in epilogues that stream X through L2.  Here one cluster of C CTAs runs
+// the whole chain of one matrix ("Muon 优化器" §2, the iteration; Algorithm 1's
+// Newton–Schulz call): CTA c keeps columns [c w, (c + 1) w) of X for all
+// iterations, the hi plane in shared memory in the 128-byte-swizzled layout the
+// tensor core reads (K-major for the Gram, MN-major for the update) and the
+// lo plane in tensor memory.  Per iteration:
+//   Gram    each CTA: the partial S_c = X_c X_c^T (M = N = 128, K = w) in TMEM,
+//           drained into its shared memory in fp32;
+//   sum     CTA c adds rows [c R, (c + 1) R) of the C partials (R = 128 / C)
+//           in rank order, read from the other CTAs' shared memory, scales
+//           them by 1/||X||^2 in the first iteration and stores them in bf16
+//           into every CTA's copy of S;
+//   poly    every CTA forms the whole P = b S + c S^2 + (a - 1) I (S^2 on the
+//           tensor core, M = N = K = 128) and its diagonal's fp32 rounding
+//           residual; all CTAs compute the same P from the same bf16 S;
+//   update  X_c' = X_c + P X_c in groups of 128 columns (two TMEM
+//           accumulators: one group's epilogue overlaps the next group's
+//           MMAs), the epilogue writing the new hi plane back into shared
+//           memory and the lo plane into tensor memory.
+// The arithmetic is that of the tiled chain's bf16 precision (S and P in
+// bf16, the shift and the residual planes as described at the top of this
+// file).  The CTAs of a cluster meet twice per iteration, at the hardware
+// cluster barrier (release / acquire): once the partials are in shared
+// memory, and once every CTA has pushed its rows of S into all the CTAs'
+// copies (remote stores, which replace a separate gather).  The last
+// iteration writes W (or the output) through the tiled update's store paths;
+// without a fused store the final iterate goes back to the workspace.  The
+// waits on the CTA's own tensor-core work are bounded; a CTA whose wait gave
+// up skips its remaining work but still meets the others at every barrier,
+// so that no barrier waits for it forever and none leaves while another may
+// read its shared memory.
+constexpr int kCcThreads = 512;        // 16 warps: TMEM lane quarter warp & 3, 32-column quarter warp >> 2
+constexpr int kCcMaxIters = 64;
+constexpr int kCcMaxCluster = 8;
+constexpr int kCcMaxW = 512;
+constexpr uint32_t kCcBlk = 128 * 128;  // a 128-row x 64-column bf16 block (16 KB)
+constexpr uint32_t kCcTmemCols = 512;   // accumulators [0, 256), lo plane [256, 256 + w / 2)
+
+struct ClusterChainParams {
+  int C, w;                   // CTAs per matrix, columns per CTA (multiple of 128, <= kCcMaxW)
+  int m_pad;
+  const __nv_bfloat16* x;     // first iterate, hi plane [batch][128][m_pad]; lo at +lo_off
+  __nv_bfloat16* xout;        // fin.mode == 0: the final iterate (its lo at +lo_off if it has one)
+  int64_t lo_off;
+  const float* inv_s;         // [batch] (1/||X||, first iteration), or nullptr
+  int iters;
+  float coef[kCcMaxIters][3];
+  FinalStore fin;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+
+__host__ __device__ constexpr size_t cc_smem_bytes(int w) {
+  return static_cast<size_t>(w / 64) * kCcBlk   // X hi
+         + 2 * kCcBlk                           // S (bf16)
+         + 2 * kCcBlk                           // partial rows sent, then P (bf16)
+         + 2 * kCcBlk                           // partial rows received; turn-around buffers
+         + 128 * 4                              // diagonal residual of P
+         + 128                                  // barriers, TMEM slot, abort flag
+         + 1024;                                // alignment
+}
+
+// 16-byte unit u of a 128-byte row r in a 128-byte-swizzled block.
+__device__ __forceinline__ uint32_t sw128(int r, int u) {
+  return static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(u) ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Bulk copy (the TMA engine) of `bytes` from this CTA's shared memory into
+// the shared memory of a CTA of the cluster, completing the bytes on that
+// CTA's mbarrier (both cluster addresses from mapa).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// The last update's W store (W <- W*decay - lr_scale*O', or O' itself into
+// the output), 16 wide columns at a time.  Wide W: the lane's 16 values are
+// consecutive in W row `row`.
+__device__ __forceinline__ void cc_fin_wide16(const FinalStore& f, const FinTile& t, int row,
+                                              int col0, const float (&v)[16]) {
+  if (t.base == nullptr || row >= t.n_real) return;
+  const bool muon = (f.mode == 1);
+  const int64_t roff = static_cast<int64_t>(row) * t.ld;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    const int j = col0 + 8 * g;
+    if (j >= t.m_real) continue;  // m_real is a multiple of 8
+    float o[8];
+    if (t.bf) {
+      uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(t.base) + roff + j);
+      if (muon) {
+        const uint4 u = *q;
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          o[k] = fmaf(-t.lr_scale, v[8 * g + k],
+                      __uint_as_float((k & 1) ? (wd[k >> 1] & 0xffff0000u) : (wd[k >> 1] << 16)) * t.decay);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = v[8 * g + k];
+      }
+      *q = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                      pack_bf16x2(o[6], o[7]));
+    } else {
+      float4* q = reinterpret_cast<float4*>(static_cast<float*>(t.base) + roff + j);
+      if (muon) {
+        const float4 a = q[0], c = q[1];
+        const float wf[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = fmaf(-t.lr_scale, v[8 * g + k], wf[k] * t.decay);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = v[8 * g + k];
+      }
+      q[0] = make_float4(o[0], o[1], o[2], o[3]);
+      q[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// Tall W (W[j][i] holds the wide element (i, j)): the warp's 32 x 16 block of
+// O' (lane = wide row row0 + lane, v[e] = wide column col0 + e) turned around
+// through the warp's 2 KB buffer (16 rows of 32 words, word c of row e at
+// c ^ e: conflict-free both ways), after which the lane holds 16 consecutive
+// elements of W row col0 + lane / 2, from wide row row0 + 16 (lane & 1).
+// Warp-collective.
+constexpr uint32_t kCcTurnBytes = 16 * 32 * 4;
+
+__device__ __forceinline__ void cc_fin_tall16(const FinalStore& f, const FinTile& t, int row0,
+                                              int col0, const float (&v)[16], float* turn,
+                                              int lane) {
+  __syncwarp();  // the buffer's previous readers are done
+#pragma unroll
+  for (int e = 0; e < 16; ++e) turn[e * 32 + (lane ^ e)] = v[e];
+  __syncwarp();
+  const int j = col0 + (lane >> 1), i0 = row0 + 16 * (lane & 1);
+  if (t.base == nullptr || j >= t.m_real || i0 >= t.n_real) return;
+  const bool muon = (f.mode == 1);
+  const int er = lane >> 1;                    // buffer row (chunk column)
+  const float* src = turn + er * 32;
+  const int64_t off = static_cast<int64_t>(j) * t.ld + i0;
+  const bool whole = i0 + 16 <= t.n_real;
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = src[(16 * (lane & 1) + 8 * g + k) ^ er];
+    if (whole) {
+      if (t.bf) {
+        uint4* q = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(t.base) + off + 8 * g);
+        if (muon) {
+          const uint4 u = *q;
+          const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = fmaf(-t.lr_scale, o[k],
+                        __uint_as_float((k & 1) ? (wd[k >> 1] & 0xffff0000u) : (wd[k >> 1] << 16)) * t.decay);
+        }
+        *q = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                        pack_bf16x2(o[6], o[7]));
+      } else {
+        float4* q = reinterpret_cast<float4*>(static_cast<float*>(t.base) + off + 8 * g);
+        if (muon) {
+          const float4 a = q[0], c = q[1];
+          const float wf[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] = fmaf(-t.lr_scale, o[k], wf[k] * t.decay);
+        }
+        q[0] = make_float4(o[0], o[1], o[2], o[3]);
+        q[1] = make_float4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int i = i0 + 8 * g + k;
+        if (i >= t.n_real) continue;
+        if (t.bf) {
+          __nv_bfloat16* e = static_cast<__nv_bfloat16*>(t.base) + off + 8 * g + k;
+          const float wv = muon ? fmaf(-t.lr_scale, o[k], __bfloat162float(*e) * t.decay) : o[k];
+          *e = __float2bfloat16_rn(wv);
+        } else {
+          float* e = static_cast<float*>(t.base) + off + 8 * g + k;
+          *e = muon ? fmaf(-t.lr_scale, o[k], *e * t.decay) : o[k];
+        }
+      }
+    }
+  }
+}
+
+// 16 columns of the update epilogue: X' = X + P X + d X (+ clo X_lo), scaled
+// by 1/||X|| in the first iteration; hi back into shared memory (units u0,
+// u0 + 1 of row `row` of block xr), lo (kLoOut) into tensor memory.
+template <bool kLoIn, bool kLoOut>
+__device__ __forceinline__ void cc_update16(uint32_t t_acc, uint32_t t_lo, uint8_t* xr, int row,
+                                            int u0, float d, float clo, float msc) {
+  uint32_t r[16], l[8];
+  tmem_ld_32x32b_x16(t_acc, r);
+  if (kLoIn) tmem_ld_32x32b_x8(t_lo, l);
+  const uint4 h0 = *reinterpret_cast<const uint4*>(xr + sw128(row, u0));
+  const uint4 h1 = *reinterpret_cast<const uint4*>(xr + sw128(row, u0 + 1));
+  tmem_ld_wait();
+  tmem_ld_tie(r);
+  if (kLoIn) tmem_ld_tie(l);
+  const uint32_t hw_in[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  uint32_t hw[8], lw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw_in[k]));
+    float v0, v1;
+    if (kLoIn) {
+      const float2 xl = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&l[k]));
+      const float xe0 = x.x + xl.x, xe1 = x.y + xl.y;
+      v0 = fmaf(d, xe0, fmaf(clo, xl.x, xe0 + __uint_as_float(r[2 * k]))) * msc;
+      v1 = fmaf(d, xe1, fmaf(clo, xl.y, xe1 + __uint_as_float(r[2 * k + 1]))) * msc;
+    } else {
+      v0 = fmaf(d, x.x, x.x + __uint_as_float(r[2 * k])) * msc;
+      v1 = fmaf(d, x.y, x.y + __uint_as_float(r[2 * k + 1])) * msc;
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    hw[k] = *reinterpret_cast<const uint32_t*>(&h);
+    if (kLoOut) {
+      const float2 f2 = __bfloat1622float2(h);
+      lw[k] = pack_bf16x2(v0 - f2.x, v1 - f2.y);
+    }
+  }
+  *reinterpret_cast<uint4*>(xr + sw128(row, u0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(xr + sw128(row, u0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  if (kLoOut) tmem_st_32x32b_x8(t_lo, lw);
+}
+
+// The update's MMAs for group g (128 columns): D[g & 1] = P X_g, A = P
+// (K-major), B = X (MN-major), eight k steps of 16; completion on `full`.
+__device__ __forceinline__ void cc_issue_update(uint32_t tmem, uint64_t dP, uint64_t dXmn, int g,
+                                                uint64_t* full) {
+  constexpr uint32_t kIdescMN = idesc_bf16_f32(128, 128, true);
+  const uint32_t d_tm = tmem + static_cast<uint32_t>((g & 1) * 128);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint64_t ad = dP + static_cast<uint64_t>(((ks >> 2) * kCcBlk + (ks & 3) * 32) >> 4);
+    const uint64_t bd = dXmn + static_cast<uint64_t>((2 * g * kCcBlk + ks * 2048) >> 4);
+    tc_mma_bf16(d_tm, ad, bd, kIdescMN, ks != 0 ? 1u : 0u);
+  }
+  tc_commit(full);
+}
+
+// The next iteration's Gram over the two X blocks of group g, accumulated in
+// TMEM columns [256, 384); completion on `done` after the last group.
+__device__ __forceinline__ void cc_issue_gram(uint32_t tmem, uint64_t dX, int g, uint64_t* done) {
+  constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      const uint64_t dd = dX + static_cast<uint64_t>(((2 * g + j) * kCcBlk + ks * 32) >> 4);
+      tc_mma_bf16(tmem + 256, dd, dd, kIdescKK, (g | j | ks) != 0 ? 1u : 0u);
+    }
+  if (done != nullptr) tc_commit(done);
+}
+
+template <int C>
+__global__ void __launch_bounds__(kCcThreads + 32, 1)
+    k_ns_cluster_chain(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ ClusterChainParams p) {
+  constexpr int R = 128 / C;  // rows of S this CTA sums
+  static_assert(R % 8 == 0, "cluster size");
+  constexpr int kItems = (R * 16 + kCcThreads - 1) / kCcThreads;  // 8-column units per thread
+  constexpr uint32_t kSlot = R * 256;  // one CTA's fp16 partial rows for one owner
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const int nb = p.w / 64, nq = p.w / 128;
+  uint8_t* sX = smem;
+  uint8_t* sS = smem + nb * kCcBlk;  // S (bf16, K-major, two blocks)
+  uint8_t* sT = sS + 2 * kCcBlk;     // partial rows to send [owner][R][128] fp16, then P
+  uint8_t* sV = sT + 2 * kCcBlk;     // partial rows received [sender][R][128] fp16;
+                                     // turn-around buffers in the last update
+  float* pdiag = reinterpret_cast<float*>(sV + 2 * kCcBlk);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pdiag + 128);
+  uint64_t* mma_bar = bars;       // Gram / polynomial MMAs done
+  uint64_t* tma_bar = bars + 1;   // first iterate loaded
+  uint64_t* ufull = bars + 2;     // [2] update accumulators full
+  uint64_t* uempty = bars + 4;    // [2] update accumulators drained (one arrival per warp)
+  uint64_t* pbar = bars + 6;      // partial rows received
+  uint64_t* sbar = bars + 7;      // rows of S received
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  constexpr int kWarps = kCcThreads / 32;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // warps 0-15 drain TMEM (lane quarter warp & 3, 32-column quarter warp >> 2);
+  // warp 16 issues the tensor-core MMAs (an issuing thread waits for each MMA
+  // to be accepted, about as long as the MMA runs)
+  const bool mma_warp = (warp == kWarps);
+  const bool mma_thread = mma_warp && lane == 0;
+  const int q = warp & 3, h4 = (warp >> 2) & 3;
+  const int row = 32 * q + lane;
+  const uint32_t rank = cluster_ctarank();
+  const int b = static_cast<int>(blockIdx.x) / C;
+  const int col_base = static_cast<int>(rank) * p.w;
+
+  if (tid == 0) {
+    mbar_init(mma_bar, 1);
+    mbar_init(tma_bar, 1);
+    mbar_init(&ufull[0], 1);
+    mbar_init(&ufull[1], 1);
+    mbar_init(&uempty[0], kWarps);
+    mbar_init(&uempty[1], kWarps);
+    mbar_init(pbar, 1);
+    mbar_init(sbar, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmX);
+  }
+  if (mma_warp) {
+    tmem_alloc(tmem_slot, kCcTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // every CTA's barriers are initialised before any copy completes on them
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(32 * q) << 16);  // this warp's lanes
+  const uint32_t t_lo = t_row + 256;
+  const uint32_t aX = smem_u32(sX), aS = smem_u32(sS), aT = smem_u32(sT), aV = smem_u32(sV);
+  constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false);
+  constexpr uint32_t kIdescMN = idesc_bf16_f32(128, 128, true);
+
+  griddep_wait();  // X and 1/||X|| come from the previous kernels
+  const float ms = p.inv_s != nullptr ? p.inv_s[b] : 1.f;
+  // ---- first iterate: hi plane by TMA (64-column boxes of 128 rows), lo
+  // plane into tensor memory (column j at TMEM column j / 2, two per word)
+  if (tid == 0) {
+    mbar_arrive_expect_tx(tma_bar, static_cast<uint32_t>(nb) * kCcBlk);
+    for (int kb = 0; kb < nb; ++kb)
+      tma_load_3d(sX + kb * kCcBlk, &tmX, tma_bar, col_base + kb * 64, 0, b);
+  }
+  const int64_t row_off = (static_cast<int64_t>(b) * 128 + row) * p.m_pad + col_base;
+  if (kLoIters > 0 && !mma_warp) {
+    for (int g = 0; g < nq; ++g) {
+      const int cs = 128 * g + 32 * h4;
+      const uint4* src = reinterpret_cast<const uint4*>(p.x + p.lo_off + row_off + cs);
+      uint32_t u[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = src[k];
+        u[4 * k] = v.x; u[4 * k + 1] = v.y; u[4 * k + 2] = v.z; u[4 * k + 3] = v.w;
+      }
+      tmem_st_32x32b_x16(t_lo + cs / 2, u);
+    }
+    tmem_st_wait();
+  }
+  const bool tma_done = mbar_wait_bounded(tma_bar, 0, abort_flag, p.status, p.timeout_ns);
+  bool ok = __syncthreads_and(tma_done) != 0;
+
+  const bool has_fin = p.fin.mode != 0;
+  FinTile ft{};
+  if (has_fin) ft = fin_tile(p.fin, b);
+  // the W this CTA's last update reads, into L2 now (it is read once, at the end)
+  if (has_fin && !mma_warp)
+    for (int g = 0; g < nq; ++g)
+      fin_prefetch(p.fin, ft, row, 32 * q, col_base + 128 * g + 32 * h4, 32, lane);
+  // the last update's turn-around buffers, one per epilogue warp
+  float* turn = reinterpret_cast<float*>(sV + (warp & 15) * kCcTurnBytes);
+  // descriptors of the operand blocks (start-address field advanced per k step)
+  const uint64_t dX = smem_desc_sw128(aX, 16, 1024);          // K-major X
+  const uint64_t dXmn = smem_desc_sw128(aX, kCcBlk, 1024);    // MN-major X
+  const uint64_t dS = smem_desc_sw128(aS, 16, 1024);
+  const uint64_t dP = smem_desc_sw128(aT, 16, 1024);
+  uint32_t mma_ph = 0, uf_ph = 0, ue_ph = 0, x_ph = 0;  // uf / ue: bit g & 1 per accumulator
+  int armed = 0;            // exchange phases armed on pbar / sbar and not yet seen complete
+  bool gram_early = false;  // this iteration's Gram was issued during the previous update
+
+  for (int it = 0; it < p.iters; ++it) {
+    const float ca = p.coef[it][0], cb = p.coef[it][1], cc = p.coef[it][2];
+    const bool first = (it == 0), last = (it + 1 == p.iters);
+    const bool fin_now = last && has_fin;
+    const bool lo_in = it < kLoIters;
+    const bool lo_out = it + 1 < kLoIters && !fin_now;
+    const float clo = lo_in ? ca - 1.f : 0.f;
+    const float msc = first ? ms : 1.f;
+    // Once the lo plane is gone its TMEM columns hold the next iteration's
+    // Gram, whose MMAs then start group by group inside this update.
+    const bool gram_next = !lo_in && !lo_out && !last;
+    const uint32_t g_acc = gram_early ? 256u : 0u;
+    if (!ok) break;
+
+    // this iteration's exchanges: C partial slots in, the other CTAs' rows of S in
+    if (tid == 0) {
+      mbar_arrive_expect_tx(pbar, static_cast<uint32_t>(C) * kSlot);
+      mbar_arrive_expect_tx(sbar, static_cast<uint32_t>(C - 1) * kSlot);
+    }
+    armed = 2;
+
+    // ---- Gram: partial S of this CTA's columns
+    if (mma_thread && !gram_early) {
+      tc_fence_after();
+      for (int kb = 0; kb < nb; ++kb)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t dd = dX + static_cast<uint64_t>((kb * kCcBlk + ks * 32) >> 4);
+          tc_mma_bf16(tmem, dd, dd, kIdescKK, (kb | ks) != 0 ? 1u : 0u);
+        }
+      tc_commit(mma_bar);
+    }
+    {
+      const bool w = mbar_wait_bounded(mma_bar, mma_ph, abort_flag, p.status, p.timeout_ns);
+      mma_ph ^= 1u;
+      ok = __syncthreads_and(w) != 0;
+      if (!ok) break;
+    }
+    if (!mma_warp) {
+      tc_fence_after();
+      // row `row`, columns [32 h4, 32 h4 + 32) of the partial, scaled by
+      // 1/||X||^2 in the first iteration (every entry is then at most the
+      // squared spectral norm of the iterate, about 1.5), in fp16, into the
+      // owner's slot of the send buffer: 16-byte units (8 columns) swizzled
+      // by row, unit u at (u & ~7) | ((u ^ row) & 7)
+      const float f = first ? ms * ms : 1.f;
+      uint8_t* dst = sT + (row / R) * kSlot + (row % R) * 256;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(t_row + g_acc + 32 * h4 + 16 * half, r);
+        tmem_ld_wait();
+        tmem_ld_tie(r);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int u = 4 * h4 + 2 * half + k;
+          const int phys = (u & ~7) | ((u ^ row) & 7);
+          *reinterpret_cast<uint4*>(dst + phys * 16) = make_uint4(
+              pack_f16x2(__uint_as_float(r[8 * k]) * f, __uint_as_float(r[8 * k + 1]) * f),
+              pack_f16x2(__uint_as_float(r[8 * k + 2]) * f, __uint_as_float(r[8 * k + 3]) * f),
+              pack_f16x2(__uint_as_float(r[8 * k + 4]) * f, __uint_as_float(r[8 * k + 5]) * f),
+              pack_f16x2(__uint_as_float(r[8 * k + 6]) * f, __uint_as_float(r[8 * k + 7]) * f));
+        }
+      }
+      fence_proxy_async_smem();  // the copies read these rows through the async proxy
+      tc_fence_before();
+    }
+    __syncthreads();
+    if (tid == 0)
+      for (int o = 0; o < C; ++o)
+        bulk_copy_to_cluster(mapa_shared_u32(aV + rank * kSlot, static_cast<uint32_t>(o)),
+                             aT + o * kSlot, kSlot, mapa_shared(pbar, static_cast<uint32_t>(o)));
+
+    // ---- sum: rows [rank R, rank R + R) of S, the C slots added in rank
+    // order in fp32, stored in bf16 (K-major, 128-byte swizzle)
+    {
+      const bool w = mbar_wait_bounded(pbar, x_ph, abort_flag, p.status, p.timeout_ns);
+      ok = __syncthreads_and(w) != 0;
+      if (!ok) break;
+      armed = 1;
+    }
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      const int i = tid + k * kCcThreads;
+      if (!mma_warp && i < R * 16) {
+        const int lr = i >> 4, u = i & 15;
+        const int r = static_cast<int>(rank) * R + lr;
+        const uint32_t off = lr * 256 + (((u & ~7) | ((u ^ r) & 7)) << 4);
+        uint4 v[C];
+#pragma unroll
+        for (int pr = 0; pr < C; ++pr) v[pr] = *reinterpret_cast<const uint4*>(sV + pr * kSlot + off);
+        float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int pr = 0; pr < C; ++pr) {
+          const uint32_t wv[4] = {v[pr].x, v[pr].y, v[pr].z, v[pr].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&wv[j]));
+            s[2 * j] += h.x;
+            s[2 * j + 1] += h.y;
+          }
+        }
+        // columns 8u .. 8u + 7: block u / 8, unit u % 8
+        *reinterpret_cast<uint4*>(sS + (u >> 3) * kCcBlk + sw128(r, u & 7)) =
+            make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                       pack_bf16x2(s[6], s[7]));
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && C > 1) {
+      // this CTA's rows of S (R rows of each block, contiguous) to every other CTA
+      for (int o = 0; o < C; ++o) {
+        if (o == static_cast<int>(rank)) continue;
+        const uint32_t bar = mapa_shared(sbar, static_cast<uint32_t>(o));
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const uint32_t off = blk * kCcBlk + rank * R * 128;
+          bulk_copy_to_cluster(mapa_shared_u32(aS + off, static_cast<uint32_t>(o)), aS + off,
+                               R * 128, bar);
+        }
+      }
+    }
+    {
+      const bool w = mbar_wait_bounded(sbar, x_ph, abort_flag, p.status, p.timeout_ns);
+      x_ph ^= 1u;
+      ok = __syncthreads_and(w) != 0;
+      if (!ok) break;
+      armed = 0;
+    }
+
+    // ---- polynomial: P = b S + c S^2 + (a - 1) I, into the send buffer
+    if (cc != 0.f) {
+      if (mma_thread) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t dd = dS + static_cast<uint64_t>(((ks >> 2) * kCcBlk + (ks & 3) * 32) >> 4);
+          tc_mma_bf16(tmem + 128, dd, dd, kIdescKK, ks != 0 ? 1u : 0u);
+        }
+        tc_commit(mma_bar);
+      }
+      const bool w = mbar_wait_bounded(mma_bar, mma_ph, abort_flag, p.status, p.timeout_ns);
+      mma_ph ^= 1u;
+      ok = __syncthreads_and(w) != 0;
+      if (!ok) break;
+      tc_fence_after();
+    }
+    if (!mma_warp) {
+      // row `row`, columns [32 h4, 32 h4 + 32): block h4 / 2, units 4 (h4 & 1) .. + 3,
+      // in two 16-column halves; the warps with q == h4 hold the diagonal
+      // (column `lane` of their chunk)
+      const uint8_t* srow = sS + (h4 >> 1) * kCcBlk;
+      uint8_t* prow = sT + (h4 >> 1) * kCcBlk;
+      const bool diag = (q == h4);
+      float s_d = 0.f, a_d = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int u0 = 4 * (h4 & 1) + 2 * half;
+        uint32_t r[16];
+        if (cc != 0.f) tmem_ld_32x32b_x16(t_row + 128 + 32 * h4 + 16 * half, r);
+        const uint4 sv0 = *reinterpret_cast<const uint4*>(srow + sw128(row, u0));
+        const uint4 sv1 = *reinterpret_cast<const uint4*>(srow + sw128(row, u0 + 1));
+        if (cc != 0.f) {
+          tmem_ld_wait();
+          tmem_ld_tie(r);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = 0u;
+        }
+        const uint32_t sw[8] = {sv0.x, sv0.y, sv0.z, sv0.w, sv1.x, sv1.y, sv1.z, sv1.w};
+        if (diag && (lane >> 4) == half) {
+          // predicated selects (an indexed read would put r in local memory)
+          uint32_t ab = 0u, sb = 0u;
+          const int idx = lane & 15;
+#pragma unroll
+          for (int e0 = 0; e0 < 16; ++e0) {
+            const uint32_t wd = sw[e0 >> 1];
+            const uint32_t sv = (e0 & 1) ? (wd & 0xffff0000u) : (wd << 16);
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %4, %5;\n\t"
+                "selp.b32 %0, %2, %0, p;\n\tselp.b32 %1, %3, %1, p;\n\t}"
+                : "+r"(ab), "+r"(sb)
+                : "r"(r[e0]), "r"(sv), "r"(e0), "r"(idx));
+          }
+          a_d = __uint_as_float(ab);
+          s_d = __uint_as_float(sb);
+        }
+        uint32_t out[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 sf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&sw[j]));
+          out[j] = pack_bf16x2(fmaf(cc, __uint_as_float(r[2 * j]), cb * sf.x),
+                               fmaf(cc, __uint_as_float(r[2 * j + 1]), cb * sf.y));
+        }
+        *reinterpret_cast<uint4*>(prow + sw128(row, u0)) = make_uint4(out[0], out[1], out[2], out[3]);
+        *reinterpret_cast<uint4*>(prow + sw128(row, u0 + 1)) = make_uint4(out[4], out[5], out[6], out[7]);
+      }
+      if (diag) {
+        const int e = lane;
+        // the (a - 1) shift on the diagonal; its fp32 rounding residual kept
+        const float vd = fmaf(cc, a_d, cb * s_d) + (ca - 1.f);
+        const __nv_bfloat16 hd = __float2bfloat16_rn(vd);
+        pdiag[row] = vd - __bfloat162float(hd);
+        *reinterpret_cast<__nv_bfloat16*>(prow + sw128(row, 4 * (h4 & 1) + (e >> 3)) + (e & 7) * 2) = hd;
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- update: X_c' = X_c + P X_c, groups of 128 columns (TMEM
+    // accumulator g & 1), MN-major B straight from the X blocks.  Warp 0's
+    // first lane issues the MMAs; every warp reports a drained accumulator
+    // on uempty and goes on to the next group.
+    if (mma_warp) {
+      // issue the first two groups, then each further group (and the next
+      // iteration's Gram over the columns just written) once every warp has
+      // drained the accumulator it reuses
+      if (lane == 0) {
+        tc_fence_after();
+        cc_issue_update(tmem, dP, dXmn, 0, &ufull[0]);
+        if (nq > 1) cc_issue_update(tmem, dP, dXmn, 1, &ufull[1]);
+        for (int g = 0; g < nq; ++g) {
+          // every group completes a phase of uempty[g & 1]; the phases not
+          // waited for here have completed before the next iteration's waits
+          const uint32_t bit = 1u << (g & 1);
+          const uint32_t par = (ue_ph & bit) ? 1u : 0u;
+          ue_ph ^= bit;
+          if (!ok || (g + 2 >= nq && !gram_next)) continue;
+          if (!mbar_wait_bounded(&uempty[g & 1], par, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            continue;
+          }
+          tc_fence_after();
+          if (g + 2 < nq) cc_issue_update(tmem, dP, dXmn, g + 2, &ufull[g & 1]);
+          if (gram_next) cc_issue_gram(tmem, dX, g, g + 1 == nq ? mma_bar : nullptr);
+        }
+      }
+      __syncwarp();
+    } else {
+      const float d = pdiag[row];
+      for (int g = 0; g < nq; ++g) {
+        const uint32_t bit = 1u << (g & 1);
+        bool w = ok && mbar_wait_bounded(&ufull[g & 1], (uf_ph & bit) ? 1u : 0u, abort_flag,
+                                         p.status, p.timeout_ns);
+        uf_ph ^= bit;
+        w = __all_sync(0xffffffffu, w);
+        ok = ok && w;
+        const int cs = 128 * g + 32 * h4;  // slice column of the thread's chunk
+        uint8_t* xr = sX + (cs >> 6) * kCcBlk;
+        const int u0 = (cs & 63) >> 3;
+        const uint32_t t_acc = t_row + (g & 1) * 128 + 32 * h4;
+        if (ok) tc_fence_after();
+        if (fin_now) {
+          // O' in two 16-column halves (the last iteration never reads the lo
+          // plane)
+          uint4 hv[4];
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) hv[k] = *reinterpret_cast<const uint4*>(xr + sw128(row, u0 + k));
+          }
+          const uint32_t* hw_in = reinterpret_cast<const uint32_t*>(hv);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float v[16];
+            if (ok) {
+              uint32_t r[16];
+              tmem_ld_32x32b_x16(t_acc + 16 * half, r);
+              tmem_ld_wait();
+              tmem_ld_tie(r);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float2 x = __bfloat1622float2(
+                    *reinterpret_cast<const __nv_bfloat162*>(&hw_in[8 * half + k]));
+                v[2 * k] = fmaf(d, x.x, x.x + __uint_as_float(r[2 * k])) * msc;
+                v[2 * k + 1] = fmaf(d, x.y, x.y + __uint_as_float(r[2 * k + 1])) * msc;
+              }
+            }
+            const int col0 = col_base + cs + 16 * half;
+            if (ft.tall) {
+              if (ok) cc_fin_tall16(p.fin, ft, 32 * q, col0, v, turn, lane);
+            } else if (ok) {
+              cc_fin_wide16(p.fin, ft, row, col0, v);
+            }
+          }
+        } else if (ok) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t ta = t_acc + 16 * half, tl = t_lo + cs / 2 + 8 * half;
+            if (lo_in && lo_out)
+              cc_update16<true, true>(ta, tl, xr, row, u0 + 2 * half, d, clo, msc);
+            else if (lo_in)
+              cc_update16<true, false>(ta, tl, xr, row, u0 + 2 * half, d, clo, msc);
+            else
+              cc_update16<false, false>(ta, tl, xr, row, u0 + 2 * half, d, clo, msc);
+          }
+        }
+        if (gram_next) fence_proxy_async_smem();  // X' blocks of group g feed the next Gram
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&uempty[g & 1]);
+      }
+    }
+    if (lo_out) tmem_st_wait();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    gram_early = gram_next;
+    ok = __syncthreads_and(ok) != 0;
+  }
+
+  // ---- the final iterate back to the workspace (no fused store)
+  if (ok && !has_fin && p.iters > 0 && !mma_warp) {
+    const bool lo = p.iters < kLoIters;
+    __nv_bfloat16* dst = p.xout + row_off;
+    for (int g = 0; g < nq; ++g) {
+      const int cs = 128 * g + 32 * h4;
+      const uint8_t* xr = sX + (cs >> 6) * kCcBlk;
+      const int u0 = (cs & 63) >> 3;
+      uint4 hv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) hv[k] = *reinterpret_cast<const uint4*>(xr + sw128(row, u0 + k));
+      st_global_v8(dst + cs, hv[0], hv[1]);
+      st_global_v8(dst + cs + 16, hv[2], hv[3]);
+      if (lo) {
+        uint32_t l[16];
+        tmem_ld_32x32b_x16(t_lo + cs / 2, l);
+        tmem_ld_wait();
+        tmem_ld_tie(l);
+        st_global_v8(dst + p.lo_off + cs, make_uint4(l[0], l[1], l[2], l[3]),
+                     make_uint4(l[4], l[5], l[6], l[7]));
+        st_global_v8(dst + p.lo_off + cs + 16, make_uint4(l[8], l[9], l[10], l[11]),
+                     make_uint4(l[12], l[13], l[14], l[15]));
+      }
+    }
+  }
+
+  // ---- teardown.  Every MMA and the first load complete; then, once all
+  // CTAs of the cluster have stopped issuing copies (the cluster barrier),
+  // the copies this CTA still expected after a wait gave up have landed
+  // (bounded waits), so that none writes into shared memory after the CTA
+  // has left it.
+  if (mma_thread) {
+    tc_commit(drain);
+    mbar_wait_drain(drain, 0, p.status, p.timeout_ns);
+  }
+  if (tid == 0) {
+    griddep_launch_dependents();
+    if (!tma_done) mbar_wait_drain(tma_bar, 0, p.status, p.timeout_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (tid == 0) {
+    if (armed == 2) mbar_wait_drain(pbar, x_ph, p.status, p.timeout_ns);
+    if (armed >= 1) mbar_wait_drain(sbar, x_ph, p.status, p.timeout_ns);
+  }
+  __syncthreads();
+  if (mma_warp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kCcTmemCols);
+  }
+}
+
 // Gram and polynomial of one iteration in one launch of the pair-wide
 // kernel (bf16 precision, c != 0).  The launch's work units are numbered by
 // tickets: every Gram unit (matrix-major) before any polynomial unit.  Each
@@ -1945,6 +2711,79 @@ cudaError_t launch_gram_poly(const CUtensorMap& x, const CUtensorMap& sk, const 
   return cudaGetLastError();
 }
 
+// Shape of the on-chip chain for a padded wide shape n_pad x m_pad: C CTAs
+// per matrix (a divisor of 128, at most kCcMaxCluster) of w columns each (a
+// multiple of 128, at most kCcMaxW), the most CTAs that fit.  A function of
+// the shape alone: a matrix's result does not depend on its batch.
+bool cluster_chain_shape(int n_pad, int m_pad, int* C, int* w) {
+  if (n_pad != kBM) return false;
+  for (int c = kCcMaxCluster; c >= 1; c >>= 1) {
+    if (m_pad % (c * 128) != 0) continue;
+    const int wc = m_pad / c;
+    if (wc > kCcMaxW) return false;
+    *C = c;
+    *w = wc;
+    return true;
+  }
+  return false;
+}
+
+// The whole chain of every matrix in one launch of k_ns_cluster_chain;
+// cudaErrorNotSupported where the GPU cannot hold one cluster of that shape.
+cudaError_t launch_cluster_chain(const CUtensorMap& tmx, const NsChainArgs& a, int C, int w,
+                                 double flops, cudaStream_t st) {
+  auto kern = C == 8 ? k_ns_cluster_chain<8>
+              : C == 4 ? k_ns_cluster_chain<4>
+              : C == 2 ? k_ns_cluster_chain<2>
+                       : k_ns_cluster_chain<1>;
+  const size_t smem = cc_smem_bytes(w);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (a.fin.mode != 0 && a.iters <= kLoIters) return cudaErrorNotSupported;
+  ClusterChainParams p{};
+  p.C = C;
+  p.w = w;
+  p.m_pad = a.m_pad;
+  p.x = a.X0;
+  p.xout = (a.iters & 1) ? a.X1 : a.X0;
+  p.lo_off = a.lo_off;
+  p.inv_s = a.inv_s;
+  p.iters = a.iters;
+  for (int it = 0; it < a.iters; ++it)
+    for (int k = 0; k < 3; ++k) p.coef[it][k] = a.coeffs[3 * it + k];
+  p.fin = a.fin;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kCcThreads + 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.gridDim = dim3(static_cast<unsigned>(C));
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorNotSupported;
+  cfg.gridDim = dim3(static_cast<unsigned>(a.batch * C));
+  if (kUsePdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  prof_begin(kKindChain, st);
+  e = cudaLaunchKernelEx(&cfg, kern, tmx, p);
+  prof_end(kKindChain, st, flops, 0.0);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Tensor maps of one operand: K-major with 128-row boxes (A, and the B half a
 // CTA of a pair loads) and BN-row boxes (unpaired B), MN-major (the update's
 // B), each for the hi and the lo plane.  Operands without a lo plane carry
@@ -2025,6 +2864,19 @@ cudaError_t run_ns_chain(const NsChainArgs& a, cudaStream_t st) {
   // otherwise 128, twice the tiles for a short-K, epilogue-bound update
   const int bn_up = (m % 256 == 0 && n % 256 == 0) ? 256 : 128;
   const bool x3 = a.x3 != 0;
+
+  // iterates of one 128-row tile: the whole chain on chip, one launch
+  int cc_c = 0, cc_w = 0;
+  if (kUseClusterChain && !x3 && a.iters <= kCcMaxIters && batch <= 65535 * 256 &&
+      cluster_chain_shape(n, m, &cc_c, &cc_w)) {
+    CUtensorMap tmx;
+    if (!map_kmajor(&tmx, a.X0, batch, n, m, kBM)) return cudaErrorInvalidValue;
+    const double nr = a.n, mr = a.m;
+    const double flops = static_cast<double>(a.iters) * batch * (3.0 * nr * nr * mr + nr * nr * nr);
+    const cudaError_t e = launch_cluster_chain(tmx, a, cc_c, cc_w, flops, st);
+    if (e != cudaErrorNotSupported) return e;
+    (void)cudaGetLastError();
+  }
 
   OperandMaps X[2], S, P;
   __nv_bfloat16* xb[2] = {a.X0, a.X1};

@@ -27,7 +27,7 @@ struct Pending {
 
 const char* const kNames[kKindCount] = {"prepare", "finalize_norm", "ns_gram", "ns_poly",
                                         "ns_update", "apply", "timeout_check", "adamw",
-                                        "ns_gram_poly"};
+                                        "ns_gram_poly", "ns_chain"};
 
 std::mutex g_mu;
 bool g_timing = false;
