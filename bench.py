@@ -610,7 +610,7 @@ def run_ours(args):
     value = job_value(args.steps, P, world, ms)
 
     # ---- per-kernel roofline (event-timed on the launching stream) --------
-    gemm = {k: prof[k] for k in ("ns_gram", "ns_poly", "ns_gram_poly", "ns_update")
+    gemm = {k: prof[k] for k in ("ns_gram", "ns_poly", "ns_gram_poly", "ns_update", "ns_chain")
             if k in prof and prof[k]["launches"]}
     ns_ms = sum(v["total_ms"] for v in gemm.values())
     ns_flops = sum(v["alg_flops"] for v in gemm.values())

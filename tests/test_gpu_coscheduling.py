@@ -65,3 +65,36 @@ def test_step_progresses_while_most_sms_are_held():
     assert busy_ms >= 190.0
     assert step_ms < busy_ms, "the step waited for the SMs to be given back"
     assert torch.equal(W2, W_solo) and torch.equal(M2, M_solo)
+
+
+def test_cluster_chain_completes_correctly_while_most_sms_are_held():
+    """The split_head set runs its whole chain as clusters of 8 CTAs that wait
+    only on one another (never on another cluster).  With all but a few SMs
+    held by a kernel on a second stream, each cluster starts once the GPU can
+    place it: the step must report no timeout (every wait limited to 50 ms)
+    and give bit for bit what it gives on an idle GPU."""
+    h = workloads.split_heads(seed=2)
+    W, G, M = h.W.to(DEV), h.G.to(DEV), h.M.to(DEV)
+    grp = [m.Group.split_head(W, G, M, h.n_heads, h.head_dim)]
+    ws = m.workspace(m.muon_step_workspace_size(grp))
+    m.muon_step_batched(grp, m.hparams(), ws)
+    code, flags = m.muon_get_status(ws)
+    assert code == m.MUON_OK and flags == 0
+    W_solo, M_solo = W.clone(), M.clone()
+
+    W2, G2, M2 = h.W.to(DEV), h.G.to(DEV), h.M.to(DEV)
+    grp2 = [m.Group.split_head(W2, G2, M2, h.n_heads, h.head_dim)]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m.muon_set_wait_timeout_ns(50_000_000)
+    busy = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(main)
+    busy.wait_event(t0)
+    m.muon_occupy_sms(sms - 24, 200 << 10, 100_000_000, stream=busy)
+    m.muon_step_batched(grp2, m.hparams(), ws)
+    torch.cuda.synchronize()
+    code, flags = m.muon_get_status(ws)
+    assert code == m.MUON_OK and flags == 0, (code, flags)
+    assert torch.equal(W2, W_solo) and torch.equal(M2, M_solo)
