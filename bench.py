@@ -34,12 +34,15 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "Muon-step params/s; Newton–Schulz TFLOP/s vs GB300 bf16 dense peak"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# default timed steps: the dense and MoE steps take 0.4-0.6 s each
+DEFAULT_STEPS = {"dense": 60, "moe": 100}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 60 dense, 100 moe, 300 otherwise: about a minute or less)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["stack", "single", "heads", "dense", "moe", "adamw"],
@@ -59,7 +62,10 @@ def parse():
                     help="dense / moe: groups of one wide shape share a Newton–Schulz chain")
     ap.add_argument("--prec", choices=["bf16", "x3"], default="bf16",
                     help="Newton–Schulz precision: bf16 (default) or split-bf16 (MUON_NS_BF16X3)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(args.workload, 300)
+    return args
 
 
 def load_peaks():
