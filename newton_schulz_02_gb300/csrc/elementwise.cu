@@ -244,16 +244,25 @@ __global__ void __launch_bounds__(kThreads) k_prepare_tall(PrepareArgs p) {
 }
 
 // ---- per-matrix norm ------------------------------------------------------------
-__global__ void k_finalize_norm(FinalizeArgs p) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= p.batch) return;
-  if (p.gp_ctr != nullptr) p.gp_ctr[b] = 0;
+// One warp per matrix: lane l adds partials l, l + 32, ... in order (double),
+// then the lanes' sums meet in a fixed shuffle tree: a fixed order that
+// depends on the partial count alone.
+__global__ void __launch_bounds__(kThreads) k_finalize_norm(FinalizeArgs p) {
+  griddep_wait();  // the partials come from the prepare pass
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int b = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (b >= p.batch) return;  // whole warps
+  if (lane == 0 && p.gp_ctr != nullptr) p.gp_ctr[b] = 0;
   int seg = 0;
   while (seg + 1 < p.nseg && b >= p.seg_begin[seg + 1]) ++seg;
   const int parts = p.seg_parts[seg];
+  const float* pp = p.partials + static_cast<int64_t>(b) * p.parts_stride;
   double s = 0.0;
-  for (int k = 0; k < parts; ++k)
-    s += static_cast<double>(p.partials[static_cast<int64_t>(b) * p.parts_stride + k]);
+  for (int k = lane; k < parts; k += 32) s += static_cast<double>(pp[k]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_down_sync(0xffffffffu, s, off);
+  if (lane != 0) return;
   if (!isfinite(s)) atomicOr(p.status, kFlagNonFinite);
   float inv;
   if (p.skip[b]) {
@@ -421,9 +430,21 @@ cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_finalize(const FinalizeArgs& a, cudaStream_t st) {
+  // a programmatic dependent of the prepare pass (it waits for its partials)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int64_t threads = static_cast<int64_t>(a.batch) * 32;
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + kThreads - 1) / kThreads));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_begin(kKindFinalize, st);
-  k_finalize_norm<<<(a.batch + 127) / 128, 128, 0, st>>>(a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_finalize_norm, a);
   prof_end(kKindFinalize, st, 0.0, static_cast<double>(a.batch) * (a.parts_stride * 4.0 + 4.0));
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
