@@ -128,3 +128,21 @@ def test_chain_step_writes_w(rows, cols, w_dtype):
             assert np.max(ulp_diff_f32(Md[b].cpu().numpy(),
                                        momentum_ref_f32(Mprev[b], G0[b], hp))) <= 1
             check_w(f64(Wd[b]), ref["W"], hp, ref["scale"], bf16=(w_dtype == torch.bfloat16))
+
+
+def test_chain_zero_input_gives_zero():
+    """1/||X|| is 0 for a zero matrix: every iteration keeps the iterate at 0."""
+    x = torch.zeros(3, 128, 2048, dtype=torch.bfloat16, device=DEV)
+    assert torch.count_nonzero(run_ns(x)).item() == 0
+
+
+def test_chain_without_normalisation_fixes_orthonormal_rows():
+    """Stable stage alone, no normalisation, on a 96 x 2048 matrix with
+    orthonormal rows: p(1) = 1 and p'(1) = 0, so the rows stay put (the
+    first iteration's Gram rows travel unscaled)."""
+    rng = np.random.default_rng(9)
+    Q, _ = np.linalg.qr(rng.standard_normal((2048, 96)))
+    x = torch.tensor(np.ascontiguousarray(Q.T[None]), dtype=torch.float32).to(DEV)
+    sched = m.Schedule([(3, (2.0, -1.5, 0.5))], normalize=False)
+    got = f64(run_ns(x, sched)[0])
+    assert rel_fro(got, Q.T) <= 1e-2
