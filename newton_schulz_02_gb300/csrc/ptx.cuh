@@ -290,24 +290,6 @@ __device__ __forceinline__ uint32_t mapa_shared_u32(uint32_t saddr, uint32_t ran
   return r;
 }
 
-// 16 bytes from the shared memory of a CTA of the cluster (distributed
-// shared memory; the address comes from mapa).
-__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t cluster_addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
-}
-
-// Orders this thread's earlier memory accesses before its later ones for
-// every thread of the cluster (used before a CTA announces data in its shared
-// memory to the other CTAs of the cluster).
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 // Bounded wait, with cluster-scope acquire, for the phase of this CTA's
 // mbarrier `bar` with the given parity (a word handed over by another CTA).
 __device__ __forceinline__ bool mbar_wait_acquire_cluster(uint64_t* bar, uint32_t parity,
