@@ -2713,16 +2713,18 @@ cudaError_t launch_gram_poly(const CUtensorMap& x, const CUtensorMap& sk, const 
 
 // Shape of the on-chip chain for a padded wide shape n_pad x m_pad: C CTAs
 // per matrix (a divisor of 128, at most kCcMaxCluster) of w columns each (a
-// multiple of 128, at most kCcMaxW), the most CTAs that fit.  A function of
-// the shape alone: a matrix's result does not depend on its batch.
+// multiple of 128, at most kCcMaxW), the fewest CTAs that fit: the exchange
+// between a cluster's CTAs costs about the same whatever their width, so wide
+// slices give the most work per exchange (a 128 x 1024 matrix on 8 CTAs of 128
+// columns ran at half the tiled chain's rate for large batches).  A function
+// of the shape alone: a matrix's result does not depend on its batch.
 bool cluster_chain_shape(int n_pad, int m_pad, int* C, int* w) {
   if (n_pad != kBM) return false;
-  for (int c = kCcMaxCluster; c >= 1; c >>= 1) {
+  for (int c = 1; c <= kCcMaxCluster; c <<= 1) {
     if (m_pad % (c * 128) != 0) continue;
-    const int wc = m_pad / c;
-    if (wc > kCcMaxW) return false;
+    if (m_pad / c > kCcMaxW) continue;
     *C = c;
-    *w = wc;
+    *w = m_pad / c;
     return true;
   }
   return false;

@@ -4,7 +4,8 @@ Wide iterates of at most 128 rows run every Newton–Schulz iteration in one
 launch: a cluster of C CTAs per matrix keeps its columns of X on chip, adds
 the CTAs' partial Grams through distributed shared memory and forms the
 polynomial and the update there.  These cases cover each cluster shape (1, 2,
-4 and 8 CTAs; 1 to 4 update groups of 128 columns per CTA), ragged rows and
+4 and 8 CTAs; 1 to 4 update groups of 128 columns per CTA; the 128-row shapes
+of the other GPU tests add 1 CTA of 128 columns), ragged rows and
 columns, both orientations of W and of the output, the lo plane's hand-over
 at the iteration counts where it stops, the fused W store of the last
 iteration, a schedule whose polynomial has c = 0, and bit-for-bit
@@ -47,14 +48,17 @@ def oracle_ns(x, stages=oracle.HYBRID_STAGES):
     return [oracle.newton_schulz(f64(x[b]), stages, True) for b in range(x.shape[0])]
 
 
-# (rows, cols) -> wide n x m: CTAs per matrix x columns per CTA
+# (rows, cols) -> wide n x m: CTAs per matrix x columns per CTA (the fewest
+# CTAs of at most 512 columns)
 #   128 x 384    1 x 384 (three update groups: the third issued after the first drains)
 #   100 x 1536   4 x 384 (ragged rows)
-#   128 x 256    2 x 128
+#   128 x 768    2 x 384
+#   128 x 1024   2 x 512
 #   64 x 4096    8 x 512
 #   4096 x 96    8 x 512 (tall: the output written transposed)
 #   120 x 3000   8 x 384 (ragged columns, m padded to 3072)
-CHAIN_SHAPES = [(128, 384), (100, 1536), (128, 256), (64, 4096), (4096, 96), (120, 3000)]
+CHAIN_SHAPES = [(128, 384), (100, 1536), (128, 768), (128, 1024), (64, 4096), (4096, 96),
+                (120, 3000)]
 
 
 @pytest.mark.parametrize("rows,cols", CHAIN_SHAPES)
