@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import time
@@ -399,11 +400,22 @@ def run_reference(args):
     return 0
 
 
+def code_only(text: str) -> str:
+    """C++/CUDA source without comments and blank lines (the files hashed hold
+    no comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(files=("ns_gemm.cu", "ptx.cuh")):
+    """sha256 (first 16 hex) of the kernel sources' code, comments aside: the
+    committed DRAM-traffic summaries hold the hash of the code they were
+    captured on."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "newton_schulz_02_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "newton_schulz_02_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -1381,32 +1381,36 @@ __global__ void __launch_bounds__(kRpThreads) k_gram_reduce_poly(const GramReduc
 // iterations, the hi plane in shared memory in the 128-byte-swizzled layout the
 // tensor core reads (K-major for the Gram, MN-major for the update) and the
 // lo plane in tensor memory.  Per iteration:
-//   Gram    each CTA: the partial S_c = X_c X_c^T (M = N = 128, K = w) in TMEM,
-//           drained into its shared memory in fp32;
-//   sum     CTA c adds rows [c R, (c + 1) R) of the C partials (R = 128 / C)
-//           in rank order, read from the other CTAs' shared memory, scales
-//           them by 1/||X||^2 in the first iteration and stores them in bf16
-//           into every CTA's copy of S;
+//   Gram    each CTA: the partial S_c = X_c X_c^T (M = N = 128, K = w) in TMEM;
+//           its rows, scaled by 1/||X||^2 in the first iteration, in fp16, go
+//           to the CTAs that own them (CTA c owns rows [c R, (c + 1) R),
+//           R = 128 / C) as one bulk copy per owner;
+//   sum     each owner adds the C partials of its rows in rank order (fp32)
+//           and sends its rows of S, in bf16, to every other CTA (bulk
+//           copies again);
 //   poly    every CTA forms the whole P = b S + c S^2 + (a - 1) I (S^2 on the
 //           tensor core, M = N = K = 128) and its diagonal's fp32 rounding
 //           residual; all CTAs compute the same P from the same bf16 S;
 //   update  X_c' = X_c + P X_c in groups of 128 columns (two TMEM
 //           accumulators: one group's epilogue overlaps the next group's
 //           MMAs), the epilogue writing the new hi plane back into shared
-//           memory and the lo plane into tensor memory.
+//           memory and the lo plane into tensor memory; once the lo plane is
+//           gone the next iteration's Gram MMAs run group by group inside
+//           the update, in the lo plane's TMEM columns.
 // The arithmetic is that of the tiled chain's bf16 precision (S and P in
 // bf16, the shift and the residual planes as described at the top of this
-// file).  The CTAs of a cluster meet twice per iteration, at the hardware
-// cluster barrier (release / acquire): once the partials are in shared
-// memory, and once every CTA has pushed its rows of S into all the CTAs'
-// copies (remote stores, which replace a separate gather).  The last
-// iteration writes W (or the output) through the tiled update's store paths;
-// without a fused store the final iterate goes back to the workspace.  The
-// waits on the CTA's own tensor-core work are bounded; a CTA whose wait gave
-// up skips its remaining work but still meets the others at every barrier,
-// so that no barrier waits for it forever and none leaves while another may
+// file).  Each bulk copy completes on an mbarrier of the receiving CTA, and
+// every buffer is reused only once the exchange order shows that its readers
+// are done.  A dedicated warp issues the MMAs (the issuing thread waits for
+// each MMA to be accepted); 16 warps drain TMEM.  The last iteration writes W
+// (or the output) directly, W prefetched into L2 when the chain starts;
+// without a fused store the final iterate goes back to the workspace.  Every
+// wait is bounded; a CTA whose wait gave up skips its remaining work, meets
+// the others at the final cluster barrier and then waits (bounded) for the
+// copies still owed to it, so that none leaves while another may write or
 // read its shared memory.
-constexpr int kCcThreads = 512;        // 16 warps: TMEM lane quarter warp & 3, 32-column quarter warp >> 2
+constexpr int kCcThreads = 512;  // drain warps: lane quarter warp & 3, 32-column quarter warp >> 2;
+                                 // the block adds one warp that issues the MMAs
 constexpr int kCcMaxIters = 64;
 constexpr int kCcMaxCluster = 8;
 constexpr int kCcMaxW = 512;

@@ -120,6 +120,16 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path):
     assert bench.read_traffic("ns_gram_poly", summary=str(tmp_path / "absent.json")) is None
 
 
+def test_kernel_hash_ignores_comments_only():
+    """The traffic summaries are keyed to the kernel code: comments and blank
+    lines do not change the hash, code does."""
+    code = "int f(int x) {\n  return x + 1;  // one\n}\n"
+    commented = "/* doc\n   more */\nint f(int x) {\n\n  return x + 1;  // another note\n}\n"
+    changed = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.code_only(code) == bench.code_only(commented)
+    assert bench.code_only(code) != bench.code_only(changed)
+
+
 def _stub_step(args):
     """Stands for one rank's bench run: joins the gloo group the spawner's
     environment describes, reduces its timed region, rank 0 prints one line."""
