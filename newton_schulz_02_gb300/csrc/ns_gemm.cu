@@ -1412,7 +1412,7 @@ __global__ void __launch_bounds__(kRpThreads) k_gram_reduce_poly(const GramReduc
 constexpr int kCcThreads = 512;  // drain warps: lane quarter warp & 3, 32-column quarter warp >> 2;
                                  // the block adds one warp that issues the MMAs
 constexpr int kCcMaxIters = 64;
-constexpr int kCcMaxCluster = 8;
+constexpr int kCcMaxCluster = 16;  // 16: a non-portable cluster size, used where the GPU places it
 constexpr int kCcMaxW = 512;
 constexpr uint32_t kCcBlk = 128 * 128;  // a 128-row x 64-column bf16 block (16 KB)
 constexpr uint32_t kCcTmemCols = 512;   // accumulators [0, 256), lo plane [256, 256 + w / 2)
@@ -2716,7 +2716,7 @@ cudaError_t launch_gram_poly(const CUtensorMap& x, const CUtensorMap& sk, const 
 }
 
 // Shape of the on-chip chain for a padded wide shape n_pad x m_pad: C CTAs
-// per matrix (a divisor of 128, at most kCcMaxCluster) of w columns each (a
+// per matrix (a power of two, at most kCcMaxCluster) of w columns each (a
 // multiple of 128, at most kCcMaxW), the fewest CTAs that fit: the exchange
 // between a cluster's CTAs costs about the same whatever their width, so wide
 // slices give the most work per exchange (a 128 x 1024 matrix on 8 CTAs of 128
@@ -2738,7 +2738,8 @@ bool cluster_chain_shape(int n_pad, int m_pad, int* C, int* w) {
 // cudaErrorNotSupported where the GPU cannot hold one cluster of that shape.
 cudaError_t launch_cluster_chain(const CUtensorMap& tmx, const NsChainArgs& a, int C, int w,
                                  double flops, cudaStream_t st) {
-  auto kern = C == 8 ? k_ns_cluster_chain<8>
+  auto kern = C == 16 ? k_ns_cluster_chain<16>
+              : C == 8 ? k_ns_cluster_chain<8>
               : C == 4 ? k_ns_cluster_chain<4>
               : C == 2 ? k_ns_cluster_chain<2>
                        : k_ns_cluster_chain<1>;
@@ -2746,6 +2747,13 @@ cudaError_t launch_cluster_chain(const CUtensorMap& tmx, const NsChainArgs& a, i
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  if (C > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return cudaErrorNotSupported;
+    }
+  }
   if (a.fin.mode != 0 && a.iters <= kLoIters) return cudaErrorNotSupported;
   ClusterChainParams p{};
   p.C = C;
@@ -2775,8 +2783,10 @@ cudaError_t launch_cluster_chain(const CUtensorMap& tmx, const NsChainArgs& a, i
   cfg.gridDim = dim3(static_cast<unsigned>(C));
   int clusters = 0;
   e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-  if (e != cudaSuccess) return e;
-  if (clusters < 1) return cudaErrorNotSupported;
+  if (e != cudaSuccess || clusters < 1) {
+    (void)cudaGetLastError();
+    return cudaErrorNotSupported;  // the tiled chain instead
+  }
   cfg.gridDim = dim3(static_cast<unsigned>(a.batch * C));
   if (kUsePdl) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

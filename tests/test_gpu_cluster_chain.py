@@ -4,7 +4,7 @@ Wide iterates of at most 128 rows run every Newton–Schulz iteration in one
 launch: a cluster of C CTAs per matrix keeps its columns of X on chip, adds
 the CTAs' partial Grams through distributed shared memory and forms the
 polynomial and the update there.  These cases cover each cluster shape (1, 2,
-4 and 8 CTAs; 1 to 4 update groups of 128 columns per CTA; the 128-row shapes
+4, 8 and 16 CTAs; 1 to 4 update groups of 128 columns per CTA; the 128-row shapes
 of the other GPU tests add 1 CTA of 128 columns), ragged rows and
 columns, both orientations of W and of the output, the lo plane's hand-over
 at the iteration counts where it stops, the fused W store of the last
@@ -57,8 +57,10 @@ def oracle_ns(x, stages=oracle.HYBRID_STAGES):
 #   64 x 4096    8 x 512
 #   4096 x 96    8 x 512 (tall: the output written transposed)
 #   120 x 3000   8 x 384 (ragged columns, m padded to 3072)
+#   128 x 8192   16 x 512 (a non-portable cluster size; the tiled chain where the
+#                GPU cannot place one)
 CHAIN_SHAPES = [(128, 384), (100, 1536), (128, 768), (128, 1024), (64, 4096), (4096, 96),
-                (120, 3000)]
+                (120, 3000), (128, 8192)]
 
 
 @pytest.mark.parametrize("rows,cols", CHAIN_SHAPES)

@@ -150,9 +150,10 @@ def test_ns_repeated_calls_bitwise(batch, rows, cols):
         assert torch.equal(run_ns(x), first)
 
 
-# Grams of at most 128 rows over a long K are split into K-slices summed by a
-# separate pass (2 slices at K = 2048, 4 at K >= 4096).
-SPLIT_SHAPES = [(128, 2048), (96, 4096), (4096, 120), (128, 8192)]
+# Grams of at most 128 rows over a long K: the on-chip chain up to K = 8192
+# (test_gpu_cluster_chain.py covers it in detail), beyond that the tiled chain,
+# whose split-K Gram adds K-slices in a separate pass (8 slices at K = 16384).
+SPLIT_SHAPES = [(128, 2048), (96, 4096), (4096, 120), (128, 8192), (128, 16384)]
 
 
 @pytest.mark.parametrize("rows,cols", SPLIT_SHAPES)
