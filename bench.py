@@ -461,11 +461,14 @@ def e2e_leg(m, stream, groups_of, grads, W_list, hp, ws, sched, n_e, world, dev,
     """End to end through host buffers, pipelined the way a training loop fed
     from host memory runs: step i's gradients (pinned host -> one of two
     device slots, on a copy stream) upload while step i - 1 computes, and step
-    i's W leaves for pinned host memory from a device snapshot taken right
-    after the step, while step i + 1 computes.  Every step's uploads and
-    downloads lie inside the timed region (the first upload waits for its
-    start, its end waits for the last download); each step's status word is
-    saved on the device and all are checked at the end.
+    i's W leaves for pinned host memory from a device snapshot (one of two, so
+    that a slow download never holds up the next snapshot) taken right after
+    the step, while step i + 1 computes.  Every step's uploads and downloads
+    lie inside the timed region (the first upload waits for its start, its end
+    waits for the last download); each step's status word is saved on the
+    device and all are checked at the end.  The first upload (pipeline fill)
+    and the last download (drain) are timed as well: they are paid once per
+    run, so their share falls with the number of steps.
     grads: per step of the input cycle, the list of gradient tensors;
     groups_of(list of gradient tensors) -> the step's muon groups."""
     import torch
@@ -477,7 +480,7 @@ def e2e_leg(m, stream, groups_of, grads, W_list, hp, ws, sched, n_e, world, dev,
         Gh.append(hs)
     slots = [[torch.empty_like(g) for g in grads[0]] for _ in range(2)]
     egs = [groups_of(sl) for sl in slots]
-    Wsnap = [torch.empty_like(w) for w in W_list]
+    Wsnap = [[torch.empty_like(w) for w in W_list] for _ in range(2)]
     Wh = pinned_like(W_list)
     status_word = ws[:4].view(torch.int32)
     flags_d = torch.zeros(n_e, dtype=torch.int32, device=dev)
@@ -492,34 +495,42 @@ def e2e_leg(m, stream, groups_of, grads, W_list, hp, ws, sched, n_e, world, dev,
         m.muon_step_batched(egs[i], hp, ws, sched)
     torch.cuda.synchronize()
     barrier()
-    t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(n_e):
-        slot = i % 2
-        with torch.cuda.stream(s_h2d):
-            s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])  # slot free again
-            for d, h in zip(slots[slot], Gh[i % len(Gh)]):
-                d.copy_(h, non_blocking=True)
-            ev_g[i].record(s_h2d)
-        stream.wait_event(ev_g[i])
-        m.muon_step_batched(egs[slot], hp, ws, sched)
-        flags_d[i:i + 1].copy_(status_word)
-        if i > 0:
-            stream.wait_event(ev_out[i - 1])  # the snapshot has left for the host
-        for d, w in zip(Wsnap, W_list):
-            d.copy_(w)
-        ev_done[i].record(stream)
-        with torch.cuda.stream(s_d2h):
-            s_d2h.wait_event(ev_done[i])
-            for h, d in zip(Wh, Wsnap):
-                h.copy_(d, non_blocking=True)
-            ev_out[i].record(s_d2h)
-    stream.wait_event(ev_out[n_e - 1])
-    flags_h.copy_(flags_d, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
+    timing = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    e0, fill_end, drain_start, drain_end, e1 = timing
+    with ClockSampler(dev.index) as clk:
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for i in range(n_e):
+            slot = i % 2
+            with torch.cuda.stream(s_h2d):
+                s_h2d.wait_event(e0 if i < 2 else ev_done[i - 2])  # slot free again
+                for d, h in zip(slots[slot], Gh[i % len(Gh)]):
+                    d.copy_(h, non_blocking=True)
+                ev_g[i].record(s_h2d)
+                if i == 0:
+                    fill_end.record(s_h2d)
+            stream.wait_event(ev_g[i])
+            m.muon_step_batched(egs[slot], hp, ws, sched)
+            flags_d[i:i + 1].copy_(status_word)
+            if i > 1:
+                stream.wait_event(ev_out[i - 2])  # this snapshot buffer has left for the host
+            for d, w in zip(Wsnap[slot], W_list):
+                d.copy_(w)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_done[i])
+                if i == n_e - 1:
+                    drain_start.record(s_d2h)
+                for h, d in zip(Wh, Wsnap[slot]):
+                    h.copy_(d, non_blocking=True)
+                ev_out[i].record(s_d2h)
+        s_d2h.wait_event(ev_out[n_e - 1])
+        drain_end.record(s_d2h)
+        stream.wait_event(ev_out[n_e - 1])
+        flags_h.copy_(flags_d, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
     barrier()
     e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     if int(flags_h.abs().sum()) != 0:
@@ -529,10 +540,13 @@ def e2e_leg(m, stream, groups_of, grads, W_list, hp, ws, sched, n_e, world, dev,
             "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in slots[0])),
             "d2h_bytes_per_step": int(sum(w.numel() * w.element_size() for w in Wh) + 4),
             "steps": n_e, "ms_per_step": e_ms / n_e, "wall_s": round(wall, 4),
+            "fill_ms": round(e0.elapsed_time(fill_end), 3),
+            "drain_ms": round(drain_start.elapsed_time(drain_end), 3),
+            "clocks": clk.summary(),
             "path": "pinned host G -> device (copy stream, overlapping the previous step), "
-                    "muon_step_batched, W snapshot on the device -> pinned host (copy "
-                    "stream, overlapping the next step); each step's status word saved "
-                    "on the device and checked after the last step"}
+                    "muon_step_batched, W snapshot on the device (two buffers) -> pinned "
+                    "host (copy stream, overlapping the next step); each step's status "
+                    "word saved on the device and checked after the last step"}
 
 
 def run_ours(args):
@@ -691,7 +705,7 @@ def run_ours(args):
     # ---- end to end: host buffers, copies inside the timed region ------------
     e2e = None
     if args.e2e_steps > 0:
-        n_e = args.e2e_steps if sets is None else max(3, min(args.e2e_steps, 8))
+        n_e = args.e2e_steps if sets is None else max(3, min(args.e2e_steps, 20))
         e2e = e2e_leg(m, stream, groups_of, step_grads, W_list, hp, ws, sched, n_e, world, dev,
                       barrier)
 
