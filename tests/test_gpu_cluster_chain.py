@@ -59,8 +59,9 @@ def oracle_ns(x, stages=oracle.HYBRID_STAGES):
 #   120 x 3000   8 x 384 (ragged columns, m padded to 3072)
 #   128 x 8192   16 x 512 (a non-portable cluster size; the tiled chain where the
 #                GPU cannot place one)
+#   96 x 6144    16 x 384
 CHAIN_SHAPES = [(128, 384), (100, 1536), (128, 768), (128, 1024), (64, 4096), (4096, 96),
-                (120, 3000), (128, 8192)]
+                (120, 3000), (128, 8192), (96, 6144)]
 
 
 @pytest.mark.parametrize("rows,cols", CHAIN_SHAPES)
@@ -112,11 +113,14 @@ def test_chain_repeated_calls_and_batch_bitwise():
 
 
 @pytest.mark.parametrize("rows,cols,w_dtype", [(96, 2048, torch.float32),
-                                               (2048, 128, torch.bfloat16)])
+                                               (2048, 128, torch.bfloat16),
+                                               (128, 8192, torch.float32),
+                                               (8192, 120, torch.bfloat16)])
 def test_chain_step_writes_w(rows, cols, w_dtype):
     """A full Muon step whose last update writes W from the cluster: wide
     fp32 W with ragged rows, and tall bf16 W (turned around through shared
-    memory); two steps with the momentum carried over."""
+    memory), on clusters of 4 and of 16 CTAs; two steps with the momentum
+    carried over."""
     W, G, M = workloads.random_case(61, rows, cols, batch=2, g_dtype=torch.float32,
                                     w_dtype=w_dtype, m_scale=5.0)
     Wd, Gd, Md = W.to(DEV), G.to(DEV), M.to(DEV)
