@@ -444,6 +444,22 @@ def pick_peak(peaks: dict, timed_s: float) -> tuple:
     return peaks["bf16_tflops"], "burst"
 
 
+def chain_memory_model(elems: float, iters: int, w_bytes: int, avg_s: float, hbm_gbs: float,
+                       dram_bytes) -> dict:
+    """The on-chip chain against the memory bound of an unfused Newton-Schulz
+    chain over the same matrices: every iteration reads the bf16 iterate
+    twice (Gram and update) and writes it once, 6 B per element, and the
+    last update reads and writes W.  `dram_bytes` is what ncu measured per
+    launch (or None)."""
+    model = elems * (6 * iters + 2 * w_bytes)
+    gbs = model / avg_s / 1e9
+    return {"model": "unfused chain: bf16 X read twice and written once per iteration, "
+                     "W read and written once",
+            "elements_per_launch": elems, "iterations": iters,
+            "alg_bytes_per_launch": model, "gbs": gbs, "frac_of_measured_copy": gbs / hbm_gbs,
+            "dram_bytes_per_launch": dram_bytes}
+
+
 def pinned_like(tensors):
     """Pinned host copies (uninitialised) of `tensors`, carved out of one
     pinned buffer."""
@@ -674,6 +690,12 @@ def run_ours(args):
                 "timing": timing, "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": None, "alg_bytes_per_launch": per_launch,
                 "avg_launch_ms": avg_s * 1e3, "peak_source": f"{peak_src} copy"}
+    if dom == "ns_chain":
+        sc = sched if sched is not None else m.muon_ns_hybrid_schedule()
+        iters = sum(sc.stages[i].steps for i in range(sc.n_stages))
+        w_bytes = (sets[names[0]][0] if sets is not None else wl["W"]).element_size()
+        roof["memory_model"] = chain_memory_model(P * prof_steps / d["launches"], iters, w_bytes,
+                                                  avg_s, peaks["hbm_gbs"], roof["traffic"])
     kernels = {}
     for k, v in timed.items():
         e = {"launches": v["launches"], "total_ms": round(v["total_ms"], 4),

@@ -120,6 +120,21 @@ def test_traffic_is_reported_only_for_the_profiled_kernel_source(tmp_path):
     assert bench.read_traffic("ns_gram_poly", summary=str(tmp_path / "absent.json")) is None
 
 
+def test_chain_memory_model_of_the_split_head_set():
+    """The split_head set (32 heads of 4096 x 128, bf16 W, ten iterations)
+    against an unfused chain's memory traffic: per head and iteration the
+    128 x 4096 iterate is read by the Gram and by the update and written
+    once; the last update reads and writes the head's W."""
+    heads, n, m, iters = 32, 128, 4096, 10
+    per_iter = heads * 3 * n * m * 2
+    w_rmw = 2 * (4096 * 4096) * 2
+    mm = bench.chain_memory_model(heads * n * m, iters, 2, 0.5e-3, 6795.1, 101e6)
+    assert mm["alg_bytes_per_launch"] == iters * per_iter + w_rmw == 1_073_741_824
+    assert abs(mm["gbs"] - 1_073_741_824 / 0.5e-3 / 1e9) < 1e-9
+    assert abs(mm["frac_of_measured_copy"] - mm["gbs"] / 6795.1) < 1e-12
+    assert mm["dram_bytes_per_launch"] == 101e6 and mm["iterations"] == 10
+
+
 def test_kernel_hash_ignores_comments_only():
     """The traffic summaries are keyed to the kernel code: comments and blank
     lines do not change the hash, code does."""
