@@ -54,7 +54,7 @@ typedef enum {
   MUON_OK = 0,
   MUON_ERR_INVALID_ARG = 1,        /* NULL where a pointer is required, bad size, bad enum */
   MUON_ERR_MISALIGNED = 2,         /* pointer not 16 B (workspace: 256 B) aligned, stride not a multiple of 8 */
-  MUON_ERR_UNSUPPORTED = 3,        /* valid request this build does not implement (e.g. TF32 NS, cols % 8) */
+  MUON_ERR_UNSUPPORTED = 3,        /* valid request the library does not implement (e.g. TF32 NS, cols % 8) */
   MUON_ERR_WORKSPACE_TOO_SMALL = 4,
   MUON_ERR_CUDA = 5,               /* a CUDA runtime call failed (no device, launch failure, ...) */
   MUON_ERR_TIMEOUT = 6             /* returned by muon_get_status when a device wait ran out */
