@@ -179,15 +179,18 @@ def test_ns_split_k_single_stage_schedules(name):
         assert rel_fro(f64(got[b]), want[b]) <= NS_TOL
 
 
-def test_long_schedule_beyond_the_fused_launch_limit():
-    """70 iterations with c != 0 on pair-wide 256 x 512 matrices: the first 64
-    Gram + polynomial pairs of the chain run as fused launches handing out
+@pytest.mark.parametrize("rows,cols", [(256, 512), (128, 2048)])
+def test_long_schedule_beyond_the_fused_launch_limit(rows, cols):
+    """70 iterations with c != 0.  On pair-wide 256 x 512 matrices the first
+    64 Gram + polynomial pairs of the chain run as fused launches handing out
     their units by tickets, the last 6 as separate Gram and polynomial
-    launches; the stable stage repeated keeps every singular value at 1, so
-    the result must still match the oracle at the bf16 bar."""
+    launches; 128 x 2048 matrices, whose chain would otherwise run on chip
+    (at most 64 iterations), take the tiled chain.  The stable stage repeated
+    keeps every singular value at 1, so the result must still match the
+    oracle at the bf16 bar."""
     stages = [(8, (3.4445, -4.7750, 2.0315)), (62, (2.0, -1.5, 0.5))]
     rng = np.random.default_rng(71)
-    x = torch.tensor(rng.standard_normal((2, 256, 512)) * 1e-3, dtype=torch.bfloat16).to(DEV)
+    x = torch.tensor(rng.standard_normal((2, rows, cols)) * 1e-3, dtype=torch.bfloat16).to(DEV)
     got = run_ns(x, m.Schedule(stages))
     want = oracle_ns_batch(x, stages)
     for b in range(2):
